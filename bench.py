@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Throughput benchmark of the KDA intra-chunk backward (tokens*heads/s, HBM roofline).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one call of the library's intra-chunk backward over the whole workload
+(the B=8, T=4096, H=16 headline case by default: 8192 units of one (batch, head,
+64-token chunk)), inputs resident in HBM.  The working set (1.61 GB read+written)
+is far larger than the 129 MB L2, so steps run back to back without an L2 flush.
+
+Under torchrun (N > 1) every rank runs its own independent shard of the same size
+(weak scaling, no collective on the data path); rank 0 prints the JSON line.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead (a
+bounded sample of the same workload per step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import kda_inputs  # noqa: E402
+
+METRIC = "KDA intra-chunk bwd tokens·heads/s and achieved HBM GB/s (B=8,T=4096,H=16)"
+UNIT = "tokens*heads/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20
+KERNEL_NAMES = {
+    "kda_intra_bwd": "kda_intra_bwd_tc_kernel",
+    "kda_intra_bwd_fp32": "kda_intra_bwd_fp32_kernel",
+}
+
+
+def algorithmic_bytes_per_unit(qk_bytes: int = 2) -> int:
+    """Bytes one unit must move at minimum: q, k, g, beta, the ten lower 16x16
+    blocks of dAqk and dAkk, and the dq, dk, dg, db outputs."""
+    bt, kd, bc = kda_inputs.BT, kda_inputs.K, 16
+    qk = 2 * bt * kd * qk_bytes
+    g = bt * kd * 4
+    beta = bt * 4
+    da = 2 * 10 * bc * bc * 4
+    out = 3 * bt * kd * 4 + bt * 4
+    return qk + g + beta + da + out
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_delta_rule_intra_gb300", "csrc")
+    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc))
+    files.append(os.path.join(ROOT, "include", "kda.h"))
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
+    try:
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("source_sha256") != source_hash():
+            return None
+        return float(fields["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_id: str):
+        self.samples = []
+        self.proc = None
+        self.device_id = device_id
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.device_id, f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.monotonic(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples or self.window is None:
+            return None
+        t0, t1 = self.window
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        note = "during timed region"
+        if not inside:  # timed region shorter than the sampling period
+            inside = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:2]
+            note = "nearest samples (timed region shorter than 100 ms)"
+        sm, mx, reasons = [], [], set()
+        for _, line in inside:
+            parts = [p.strip() for p in line.split(",")]
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(self.REASONS, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm), "note": note}
+
+
+def device_selector(dev: torch.device) -> str:
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        return str(dev.index or 0)
+
+
+def setup_dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def config_dict(cfg, path):
+    return {
+        "workload": cfg.name, "B": cfg.B, "T": cfg.T, "H": cfg.H, "K": kda_inputs.K,
+        "BT": kda_inputs.BT, "BC": 16, "units": cfg.units,
+        "qk_dtype": str(cfg.qk_dtype).replace("torch.", ""),
+        "gate_lo": cfg.gate_lo, "entry_point": path,
+        "l2": "no flush: inputs+outputs of one step (%.2f GB) exceed the 129 MB L2"
+              % (cfg.units * algorithmic_bytes_per_unit() / 1e9),
+    }
+
+
+# --------------------------------------------------------------------------- oracle
+
+def oracle_rate(cpu_inputs, units_sample, bt=64):
+    """Time the fp64 oracle on a sample; returns (tokens*heads/s, seconds, cores)."""
+    import oracle
+    lib = oracle.load()
+    t = time.perf_counter()
+    oracle.intra_bwd(*(cpu_inputs[n] for n in ("q", "k", "g", "beta", "dAqk", "dAkk")),
+                     lib=lib)
+    dt = time.perf_counter() - t
+    return units_sample * bt / dt, dt, oracle.max_threads(lib)
+
+
+def cpu_baseline(cpu, cfg):
+    """The oracle as it stands on the host cores: the first half of the batch."""
+    nb = max(1, cfg.B // 2)
+    sample = {n: v[:nb] for n, v in cpu.items()}
+    units = nb * cfg.H * (cfg.T // kda_inputs.BT)
+    value, secs, cores = oracle_rate(sample, units)
+    return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"batch elements 0..{nb - 1} of {cfg.B} ({units} of {cfg.units} "
+                      f"units), one pass, {secs:.2f} s wall on {cores} threads"}
+
+
+def sampled_check(cpu, cfg, outs, n_units=8):
+    """max|err|/max|ref| per output on a few sampled units of the last timed step."""
+    import numpy as np
+
+    import oracle
+    units = kda_inputs.sample_units(cfg, n_units)
+    sub = kda_inputs.gather_units(cpu, units, cfg.H, cfg.T)
+    ref = oracle.intra_bwd(*(sub[n] for n in ("q", "k", "g", "beta", "dAqk", "dAkk")))
+    bt = kda_inputs.BT
+    res = {}
+    for name, x, r in zip(("dq", "dk", "db", "dg"), outs, ref):
+        got = torch.stack([x[b, c * bt:(c + 1) * bt, h] for (b, h, c) in units])
+        got = got.unsqueeze(2).double().cpu().numpy()
+        res[name] = float(np.max(np.abs(got - r)) / np.max(np.abs(r)))
+    res["units"] = len(units)
+    return res
+
+
+def run_reference(args, cfg):
+    world, rank, _ = setup_dist()
+    if rank != 0:
+        return
+    import oracle
+    oracle.load()
+    cpu = kda_inputs.make_config_inputs(args.config)
+    nchunk = cfg.T // kda_inputs.BT
+    # calibrate, then size each step so the whole run stays within ~2 minutes
+    cal_units = kda_inputs.sample_units(cfg, 32)
+    cal = kda_inputs.gather_units(cpu, cal_units, cfg.H, cfg.T)
+    rate_units = oracle_rate(cal, len(cal_units))[0] / kda_inputs.BT
+    per_step = int(max(1, min(cfg.units, 120.0 * rate_units / (args.steps + args.warmup))))
+    # a contiguous run of whole (batch, chunk) rows: every head of the first chunks
+    chunks = max(1, per_step // cfg.H)
+    nb = min(cfg.B, (chunks + nchunk - 1) // nchunk)
+    sample = {n: v[:nb, : min(cfg.T, chunks * kda_inputs.BT)] for n, v in cpu.items()}
+    units = sample["q"].shape[0] * (sample["q"].shape[1] // kda_inputs.BT) * cfg.H
+    for _ in range(args.warmup):
+        oracle_rate(sample, units)
+    times = []
+    for _ in range(args.steps):
+        times.append(oracle_rate(sample, units)[1])
+    secs = sum(times)
+    value = args.steps * units * kda_inputs.BT / secs
+    cores = oracle.max_threads()
+    desc = (f"{units} of {cfg.units} units per step (batch 0..{nb - 1}, first "
+            f"{sample['q'].shape[1]} tokens, all heads)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(cfg, "oracle.intra_bwd (fp64 C, OpenMP)"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- ours
+
+def run_ours(args, cfg):
+    world, rank, local = setup_dist()
+    import gated_delta_rule_intra_gb300 as kda
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    kda.load_library()
+    stream = torch.cuda.current_stream(dev)
+    seed = kda_inputs.SEED0 + args.config + 1000 * rank
+    cpu = kda_inputs.make_inputs(cfg.B, cfg.T, cfg.H, gate_lo=cfg.gate_lo,
+                                 qk_dtype=cfg.qk_dtype, seed=seed)
+    x = {n: v.to(dev) for n, v in cpu.items()}
+    fn = getattr(kda, args.path)
+    ins = [x[n] for n in ("q", "k", "g", "beta", "dAqk", "dAkk")]
+    outs = kda._outputs(x["q"], None, None, None, None)
+
+    def step():
+        fn(*ins, *outs, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    sampler = ClockSampler(device_selector(dev))
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.monotonic()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.monotonic()
+    barrier(world)
+    sampler.window = (t0, t1)
+    time.sleep(0.25)
+    sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(ms, world, dev)
+    ms_per_step = ms_max / args.steps
+
+    # end to end through the host-buffer entry point
+    e2e = None
+    if not args.no_e2e:
+        pin = {n: v.pin_memory() for n, v in cpu.items()}
+        hout = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
+        ws = torch.empty(kda.kda_intra_bwd_host_workspace_bytes(cfg.B, cfg.T, cfg.H,
+                                                                 cfg.qk_dtype),
+                         dtype=torch.uint8, device=dev)
+        hin = [pin[n] for n in ("q", "k", "g", "beta", "dAqk", "dAkk")]
+        for _ in range(2):
+            kda.kda_intra_bwd_host(*hin, *hout, workspace=ws, stream=stream)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            kda.kda_intra_bwd_host(*hin, *hout, workspace=ws, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": world * cfg.tokens_heads * args.e2e_steps / (e_ms / 1e3),
+               "unit": UNIT,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout),
+               "steps": args.e2e_steps,
+               "entry_point": "kda_intra_bwd_host (pinned host buffers)"}
+        del ws
+
+    cpu_base = None
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        cpu_base = cpu_baseline(cpu, cfg)
+        cpu_base["parity_check"] = sampled_check(cpu, cfg, outs)
+
+    if rank != 0:
+        return
+    bytes_per_launch = cfg.units * algorithmic_bytes_per_unit(
+        torch.tensor([], dtype=cfg.qk_dtype).element_size())
+    achieved = bytes_per_launch / (ms / args.steps / 1e3) / 1e9
+    peak, peak_kind = hbm_peak()
+    kname = KERNEL_NAMES[args.path]
+    traffic = ncu_traffic(kname, cfg.name)
+    line = {
+        "metric": METRIC,
+        "value": world * cfg.tokens_heads / (ms_per_step / 1e3),
+        "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32" if args.path.endswith("fp32") else "tf32+f32",
+        "data": "synthetic", "config": config_dict(cfg, args.path),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "kernel": kname, "algorithmic_bytes_per_launch": bytes_per_launch},
+        "cpu_baseline": cpu_base,
+        "clocks": sampler.summary(),
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    p = argparse.ArgumentParser(description=__doc__,
+                                formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--config", type=int, default=2, help="workload index (2 = headline)")
+    p.add_argument("--path", choices=tuple(KERNEL_NAMES), default="kda_intra_bwd")
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    cfg = kda_inputs.CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

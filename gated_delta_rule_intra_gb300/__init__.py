@@ -1,0 +1,196 @@
+"""Python binding of libkda, the sm_103a KDA intra-chunk backward.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libkda.so`` (built in-tree by ``build.build_library()``).  There is
+no CPU or framework fallback; if the library is missing every call raises.
+
+The functions carry the C names of ``include/kda.h``:
+
+* ``kda_intra_bwd``       -- fast path (TF32 tensor-core cross terms)
+* ``kda_intra_bwd_fp32``  -- all-FP32 path
+* ``kda_intra_bwd_host``  -- host buffers in and out, copies on the stream
+* ``kda_status_str``, ``kda_abi_version``
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkda.so")
+
+KDA_OK = 0
+KDA_BF16 = 0
+KDA_FP16 = 1
+BT = 64
+K = 128
+
+_DTYPES = {torch.bfloat16: KDA_BF16, torch.float16: KDA_FP16}
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code: int, fn: str):
+        self.code = code
+        super().__init__(f"{fn} failed: {kda_status_str(code)} (status {code})")
+
+
+def load_library(path: str | None = None):
+    """Load libkda.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"{p} is missing: build it with gated_delta_rule_intra_gb300.build."
+            "build_library() (or __graft_entry__.build()); there is no fallback")
+    lib = ctypes.CDLL(p)
+    vp, fp, i, st = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int
+    sig = [vp, vp, fp, fp, fp, fp, fp, fp, fp, fp, i, i, i, i, vp]
+    for name in ("kda_intra_bwd", "kda_intra_bwd_fp32"):
+        f = getattr(lib, name)
+        f.argtypes = sig
+        f.restype = st
+    lib.kda_intra_bwd_host.argtypes = sig[:-1] + [vp, ctypes.c_size_t, vp]
+    lib.kda_intra_bwd_host.restype = st
+    lib.kda_intra_bwd_host_workspace_bytes.argtypes = [i, i, i, i]
+    lib.kda_intra_bwd_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.kda_status_str.argtypes = [i]
+    lib.kda_status_str.restype = ctypes.c_char_p
+    lib.kda_abi_version.argtypes = []
+    lib.kda_abi_version.restype = i
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def kda_status_str(code: int) -> str:
+    return load_library().kda_status_str(int(code)).decode()
+
+
+def kda_abi_version() -> int:
+    return load_library().kda_abi_version()
+
+
+def _shape(q):
+    if q.dim() != 4 or q.shape[-1] != K:
+        raise ValueError(f"q must be [B, T, H, {K}], got {tuple(q.shape)}")
+    return q.shape[0], q.shape[1], q.shape[2]
+
+
+def _check(name, t, shape, dtype, device):
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _outputs(q, dq, dk, db, dg):
+    B, T, H = _shape(q)
+    f32 = torch.float32
+    dq = torch.empty(B, T, H, K, device=q.device, dtype=f32) if dq is None else dq
+    dk = torch.empty(B, T, H, K, device=q.device, dtype=f32) if dk is None else dk
+    dg = torch.empty(B, T, H, K, device=q.device, dtype=f32) if dg is None else dg
+    db = torch.empty(B, T, H, device=q.device, dtype=f32) if db is None else db
+    return dq, dk, db, dg
+
+
+def _validate(q, k, g, beta, dAqk, dAkk, dq, dk, db, dg, device):
+    B, T, H = _shape(q)
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"q/k dtype must be bf16 or fp16, got {q.dtype}")
+    f32 = torch.float32
+    _check("q", q, (B, T, H, K), q.dtype, device)
+    _check("k", k, (B, T, H, K), q.dtype, device)
+    _check("g", g, (B, T, H, K), f32, device)
+    _check("beta", beta, (B, T, H), f32, device)
+    _check("dAqk", dAqk, (B, T, H, BT), f32, device)
+    _check("dAkk", dAkk, (B, T, H, BT), f32, device)
+    for n, t in (("dq", dq), ("dk", dk), ("dg", dg)):
+        _check(n, t, (B, T, H, K), f32, device)
+    _check("db", db, (B, T, H), f32, device)
+    return B, T, H
+
+
+def _stream_handle(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else stream)
+
+
+def _device_call(fn_name, q, k, g, beta, dAqk, dAkk, dq, dk, db, dg, stream):
+    if q.device.type != "cuda":
+        raise ValueError(f"{fn_name} needs CUDA tensors (no CPU path exists)")
+    dq, dk, db, dg = _outputs(q, dq, dk, db, dg)
+    B, T, H = _validate(q, k, g, beta, dAqk, dAkk, dq, dk, db, dg, q.device)
+    lib = load_library()
+    ptr = ctypes.c_void_p
+    with torch.cuda.device(q.device):
+        rc = getattr(lib, fn_name)(
+            ptr(q.data_ptr()), ptr(k.data_ptr()), ptr(g.data_ptr()), ptr(beta.data_ptr()),
+            ptr(dAqk.data_ptr()), ptr(dAkk.data_ptr()), ptr(dq.data_ptr()),
+            ptr(dk.data_ptr()), ptr(db.data_ptr()), ptr(dg.data_ptr()),
+            B, T, H, _DTYPES[q.dtype], _stream_handle(stream, q.device))
+    if rc != KDA_OK:
+        raise KdaError(rc, fn_name)
+    return dq, dk, db, dg
+
+
+def kda_intra_bwd(q, k, g, beta, dAqk, dAkk, dq=None, dk=None, db=None, dg=None,
+                  stream=None):
+    """Intra-chunk backward (fast path).  Returns (dq, dk, db, dg), all fp32.
+
+    Tensors: q, k [B,T,H,128] bf16/fp16; g [B,T,H,128] fp32 chunk-local cumulative
+    log2 gate; beta [B,T,H] fp32; dAqk, dAkk [B,T,H,64] fp32.  Outputs may be passed
+    in (contiguous fp32) or are allocated.  Runs on ``stream`` (default: current).
+    """
+    return _device_call("kda_intra_bwd", q, k, g, beta, dAqk, dAkk, dq, dk, db, dg, stream)
+
+
+def kda_intra_bwd_fp32(q, k, g, beta, dAqk, dAkk, dq=None, dk=None, db=None, dg=None,
+                       stream=None):
+    """Same contract as ``kda_intra_bwd``; every product and sum in FP32."""
+    return _device_call("kda_intra_bwd_fp32", q, k, g, beta, dAqk, dAkk, dq, dk, db, dg,
+                        stream)
+
+
+def kda_intra_bwd_host_workspace_bytes(B: int, T: int, H: int, qk_dtype=torch.bfloat16):
+    return load_library().kda_intra_bwd_host_workspace_bytes(B, T, H, _DTYPES[qk_dtype])
+
+
+def kda_intra_bwd_host(q, k, g, beta, dAqk, dAkk, dq, dk, db, dg, workspace, stream=None):
+    """Host tensors in and out (pin them for asynchronous copies).
+
+    ``workspace`` is a CUDA uint8 tensor of at least
+    ``kda_intra_bwd_host_workspace_bytes(B, T, H, q.dtype)`` bytes.  The call queues
+    the copies and the kernel on ``stream`` and returns; synchronise the stream
+    before reading dq/dk/db/dg.
+    """
+    for n, t in (("q", q), ("k", k), ("g", g), ("beta", beta), ("dAqk", dAqk),
+                 ("dAkk", dAkk), ("dq", dq), ("dk", dk), ("db", db), ("dg", dg)):
+        if t.device.type != "cpu":
+            raise ValueError(f"{n} must be a host tensor")
+    B, T, H = _validate(q, k, g, beta, dAqk, dAkk, dq, dk, db, dg, torch.device("cpu"))
+    if workspace.device.type != "cuda":
+        raise ValueError("workspace must be device memory")
+    lib = load_library()
+    ptr = ctypes.c_void_p
+    nbytes = workspace.numel() * workspace.element_size()
+    with torch.cuda.device(workspace.device):
+        rc = lib.kda_intra_bwd_host(
+            ptr(q.data_ptr()), ptr(k.data_ptr()), ptr(g.data_ptr()), ptr(beta.data_ptr()),
+            ptr(dAqk.data_ptr()), ptr(dAkk.data_ptr()), ptr(dq.data_ptr()),
+            ptr(dk.data_ptr()), ptr(db.data_ptr()), ptr(dg.data_ptr()),
+            B, T, H, _DTYPES[q.dtype], ptr(workspace.data_ptr()), nbytes,
+            _stream_handle(stream, workspace.device))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_intra_bwd_host")
+    return dq, dk, db, dg

@@ -1,0 +1,209 @@
+// C ABI of libkda: argument validation and dispatch (see include/kda.h).
+#include <stdint.h>
+#include <string.h>
+
+#include <cuda_runtime.h>
+
+#include "../../include/kda.h"
+#include "kda_launch.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+// 0 = unknown, 1 = supported (cc 10.3), 2 = unsupported.  Written once per device;
+// a benign race writes the same value twice.
+volatile int g_device_ok[kMaxDevices];
+
+struct Range {
+    uintptr_t lo, hi;
+};
+
+bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+kda_status_t check_shape(int B, int T, int H) {
+    if (B <= 0 || T <= 0 || H <= 0) return KDA_ERR_SHAPE;
+    if (T % KDA_BT != 0) return KDA_ERR_SHAPE;
+    const long long rows = (long long)B * T * H;
+    const long long units = rows / KDA_BT;
+    if (units > 0x7fffffffLL) return KDA_ERR_SHAPE;     // grid limit
+    if (rows > (1LL << 52) / KDA_K) return KDA_ERR_SHAPE; // index arithmetic headroom
+    return KDA_OK;
+}
+
+kda_status_t check_args(const void *q, const void *k, const float *g, const float *beta,
+                        const float *dAqk, const float *dAkk, float *dq, float *dk,
+                        float *db, float *dg, int B, int T, int H, kda_dtype_t dt,
+                        bool device_alignment) {
+    if (!q || !k || !g || !beta || !dAqk || !dAkk || !dq || !dk || !db || !dg)
+        return KDA_ERR_NULL;
+    kda_status_t st = check_shape(B, T, H);
+    if (st != KDA_OK) return st;
+    if (dt != KDA_BF16 && dt != KDA_FP16) return KDA_ERR_DTYPE;
+    if (device_alignment) {
+        const void *a16[] = {q, k, g, dAqk, dAkk, dq, dk, dg};
+        for (const void *p : a16)
+            if ((uintptr_t)p % 16u) return KDA_ERR_ALIGN;
+        if ((uintptr_t)beta % 4u || (uintptr_t)db % 4u) return KDA_ERR_ALIGN;
+    }
+    const size_t rows = (size_t)B * T * H;
+    const Range in[] = {
+        {(uintptr_t)q, (uintptr_t)q + rows * KDA_K * 2},
+        {(uintptr_t)k, (uintptr_t)k + rows * KDA_K * 2},
+        {(uintptr_t)g, (uintptr_t)g + rows * KDA_K * 4},
+        {(uintptr_t)beta, (uintptr_t)beta + rows * 4},
+        {(uintptr_t)dAqk, (uintptr_t)dAqk + rows * KDA_BT * 4},
+        {(uintptr_t)dAkk, (uintptr_t)dAkk + rows * KDA_BT * 4},
+    };
+    const Range out[] = {
+        {(uintptr_t)dq, (uintptr_t)dq + rows * KDA_K * 4},
+        {(uintptr_t)dk, (uintptr_t)dk + rows * KDA_K * 4},
+        {(uintptr_t)db, (uintptr_t)db + rows * 4},
+        {(uintptr_t)dg, (uintptr_t)dg + rows * KDA_K * 4},
+    };
+    for (int o = 0; o < 4; ++o) {
+        for (const Range &r : in)
+            if (overlaps(out[o], r)) return KDA_ERR_OVERLAP;
+        for (int p = o + 1; p < 4; ++p)
+            if (overlaps(out[o], out[p])) return KDA_ERR_OVERLAP;
+    }
+    return KDA_OK;
+}
+
+kda_status_t check_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevices && g_device_ok[dev] != 0)
+        return g_device_ok[dev] == 1 ? KDA_OK : KDA_ERR_UNSUPPORTED_DEVICE;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    const bool ok = (major == 10 && minor == 3);
+    if (dev >= 0 && dev < kMaxDevices) g_device_ok[dev] = ok ? 1 : 2;
+    return ok ? KDA_OK : KDA_ERR_UNSUPPORTED_DEVICE;
+}
+
+kda::BwdArgs pack(const void *q, const void *k, const float *g, const float *beta,
+                  const float *dAqk, const float *dAkk, float *dq, float *dk, float *db,
+                  float *dg, int B, int T, int H, kda_dtype_t dt) {
+    kda::BwdArgs a;
+    a.q = q; a.k = k; a.g = g; a.beta = beta; a.dAqk = dAqk; a.dAkk = dAkk;
+    a.dq = dq; a.dk = dk; a.db = db; a.dg = dg;
+    a.B = B; a.T = T; a.H = H;
+    a.fp16 = (dt == KDA_FP16);
+    return a;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+extern "C" {
+
+kda_status_t kda_intra_bwd_fp32(const void *q, const void *k, const float *g,
+                                const float *beta, const float *dAqk, const float *dAkk,
+                                float *dq, float *dk, float *db, float *dg, int B, int T,
+                                int H, kda_dtype_t qk_dtype, kda_stream_t stream) {
+    kda_status_t st = check_args(q, k, g, beta, dAqk, dAkk, dq, dk, db, dg, B, T, H,
+                                 qk_dtype, true);
+    if (st != KDA_OK) return st;
+    if ((st = check_device()) != KDA_OK) return st;
+    (void)cudaGetLastError();  // launch errors below must be this call's own
+    const kda::BwdArgs a = pack(q, k, g, beta, dAqk, dAkk, dq, dk, db, dg, B, T, H, qk_dtype);
+    return kda::launch_intra_fp32(a, (cudaStream_t)stream) == cudaSuccess ? KDA_OK
+                                                                          : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_intra_bwd(const void *q, const void *k, const float *g, const float *beta,
+                           const float *dAqk, const float *dAkk, float *dq, float *dk,
+                           float *db, float *dg, int B, int T, int H, kda_dtype_t qk_dtype,
+                           kda_stream_t stream) {
+    kda_status_t st = check_args(q, k, g, beta, dAqk, dAkk, dq, dk, db, dg, B, T, H,
+                                 qk_dtype, true);
+    if (st != KDA_OK) return st;
+    if ((st = check_device()) != KDA_OK) return st;
+    (void)cudaGetLastError();
+    const kda::BwdArgs a = pack(q, k, g, beta, dAqk, dAkk, dq, dk, db, dg, B, T, H, qk_dtype);
+    return kda::launch_intra_tc(a, (cudaStream_t)stream) == cudaSuccess ? KDA_OK
+                                                                        : KDA_ERR_CUDA;
+}
+
+size_t kda_intra_bwd_host_workspace_bytes(int B, int T, int H, kda_dtype_t qk_dtype) {
+    if (check_shape(B, T, H) != KDA_OK) return 0;
+    if (qk_dtype != KDA_BF16 && qk_dtype != KDA_FP16) return 0;
+    const size_t rows = (size_t)B * T * H;
+    return 2 * align256(rows * KDA_K * 2)        /* q, k */
+           + 4 * align256(rows * KDA_K * 4)      /* g, dq, dk, dg */
+           + 2 * align256(rows * 4)              /* beta, db */
+           + 2 * align256(rows * KDA_BT * 4);    /* dAqk, dAkk */
+}
+
+kda_status_t kda_intra_bwd_host(const void *q, const void *k, const float *g,
+                                const float *beta, const float *dAqk, const float *dAkk,
+                                float *dq, float *dk, float *db, float *dg, int B, int T,
+                                int H, kda_dtype_t qk_dtype, void *workspace,
+                                size_t workspace_bytes, kda_stream_t stream) {
+    kda_status_t st = check_args(q, k, g, beta, dAqk, dAkk, dq, dk, db, dg, B, T, H,
+                                 qk_dtype, false);
+    if (st != KDA_OK) return st;
+    const size_t need = kda_intra_bwd_host_workspace_bytes(B, T, H, qk_dtype);
+    if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
+    if ((uintptr_t)workspace % 256u) return KDA_ERR_ALIGN;
+    if ((st = check_device()) != KDA_OK) return st;
+    (void)cudaGetLastError();
+
+    const size_t rows = (size_t)B * T * H;
+    const size_t nqk = rows * KDA_K * 2, nk4 = rows * KDA_K * 4, nrow = rows * 4,
+                 nda = rows * KDA_BT * 4;
+    char *w = (char *)workspace;
+    char *dq_d = w;                 w += align256(nk4);
+    char *dk_d = w;                 w += align256(nk4);
+    char *dg_d = w;                 w += align256(nk4);
+    char *db_d = w;                 w += align256(nrow);
+    char *q_d = w;                  w += align256(nqk);
+    char *k_d = w;                  w += align256(nqk);
+    char *g_d = w;                  w += align256(nk4);
+    char *beta_d = w;               w += align256(nrow);
+    char *aqk_d = w;                w += align256(nda);
+    char *akk_d = w;
+    cudaStream_t s = (cudaStream_t)stream;
+    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+    if (cudaMemcpyAsync(q_d, q, nqk, h2d, s) != cudaSuccess ||
+        cudaMemcpyAsync(k_d, k, nqk, h2d, s) != cudaSuccess ||
+        cudaMemcpyAsync(g_d, g, nk4, h2d, s) != cudaSuccess ||
+        cudaMemcpyAsync(beta_d, beta, nrow, h2d, s) != cudaSuccess ||
+        cudaMemcpyAsync(aqk_d, dAqk, nda, h2d, s) != cudaSuccess ||
+        cudaMemcpyAsync(akk_d, dAkk, nda, h2d, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    st = kda_intra_bwd(q_d, k_d, (const float *)g_d, (const float *)beta_d,
+                       (const float *)aqk_d, (const float *)akk_d, (float *)dq_d,
+                       (float *)dk_d, (float *)db_d, (float *)dg_d, B, T, H, qk_dtype,
+                       stream);
+    if (st != KDA_OK) return st;
+    if (cudaMemcpyAsync(dq, dq_d, nk4, d2h, s) != cudaSuccess ||
+        cudaMemcpyAsync(dk, dk_d, nk4, d2h, s) != cudaSuccess ||
+        cudaMemcpyAsync(dg, dg_d, nk4, d2h, s) != cudaSuccess ||
+        cudaMemcpyAsync(db, db_d, nrow, d2h, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+const char *kda_status_str(kda_status_t status) {
+    switch (status) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_NULL: return "KDA_ERR_NULL: a required pointer is NULL";
+        case KDA_ERR_SHAPE: return "KDA_ERR_SHAPE: need B,T,H > 0 and T % 64 == 0";
+        case KDA_ERR_DTYPE: return "KDA_ERR_DTYPE: qk_dtype must be KDA_BF16 or KDA_FP16";
+        case KDA_ERR_ALIGN: return "KDA_ERR_ALIGN: a pointer is misaligned";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA call or kernel launch failed";
+        case KDA_ERR_UNSUPPORTED_DEVICE:
+            return "KDA_ERR_UNSUPPORTED_DEVICE: needs compute capability 10.3 (sm_103a)";
+        case KDA_ERR_OVERLAP: return "KDA_ERR_OVERLAP: argument buffers overlap";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing or too small";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+int kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+}  // extern "C"

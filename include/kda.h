@@ -1,0 +1,135 @@
+/*
+ * libkda -- intra-chunk backward of chunked KDA (Kimi Delta Attention, the gated
+ * delta rule with a per-channel gate) on sm_103a.
+ *
+ * What it computes (bwd_intra page: the module docstring of kernel_fun/kda/_kernels/
+ * bwd_intra.py, its diagonal and epilogue loops, and the host wrapper's tensor
+ * contract).  Tokens are cut into chunks of KDA_BT = 64; a "unit" is one
+ * (batch b, head h, chunk c).  Inside a unit, with rows r, s in [0, 64), channels
+ * d in [0, 128) and E[r,s,d] = 2^(g[r,d] - g[s,d]):
+ *
+ *   Aqk[r,s] = sum_d q[r,d] k[s,d] E[r,s,d]             (s <= r)
+ *   Akk[r,s] = beta[r] * sum_d k[r,d] k[s,d] E[r,s,d]   (s <  r)
+ *
+ * Given the upstream gradients dAqk and dAkk, the library returns the gradients
+ * of L = sum dAqk*Aqk + sum dAkk*Akk with respect to q, k, beta and g:
+ *
+ *   dq[r]   = sum_{s<=r} dAqk[r,s] k[s] E[r,s]
+ *   dk[t]   = beta[t] sum_{s<t} dAkk[t,s] k[s] E[t,s]
+ *             + sum_{r>=t} (dAqk[r,t] q[r] + [r>t] dAkk[r,t] beta[r] k[r]) E[r,t]
+ *   db[r]   = sum_{s<r} dAkk[r,s] sum_d k[r,d] k[s,d] E[r,s,d]
+ *   dg[t]   = ln2 * ( q[t] (dq[t]) + (beta[t] acck[t] - dkt[t]) k[t] )
+ *             where acck[t] = sum_{s<t} dAkk[t,s] k[s] E[t,s] and dkt[t] is the
+ *             second line of dk[t]  (all products per channel d)
+ *
+ * dg is the gradient with respect to g exactly as passed (a log2 cumulative gate):
+ * it is the bwd_intra page's epilogue value times ln2.  A caller whose gate lives
+ * in natural-log units (g_nat = g * ln2) gets dL/dg_nat as dg / ln2.
+ *
+ * Supported shapes: K = 128 (head dimension), chunk 64, fixed-length sequences with
+ * T a multiple of 64 (the page's fast path; its varlen / odd-shape fallback does not
+ * exist here and such calls are rejected).  g must be the inclusive chunk-local
+ * cumulative sum of per-step log2 gates that are <= 0 (non-increasing inside each
+ * chunk): every exponent the kernels evaluate is then <= 0.
+ *
+ * Memory: every pointer is caller-owned DEVICE memory (except the *_host entry
+ * point), contiguous row-major, 16-byte aligned, and must not overlap another
+ * argument:
+ *   q, k        [B, T, H, 128]  bf16 or fp16 (qk_dtype)
+ *   g           [B, T, H, 128]  fp32
+ *   beta        [B, T, H]       fp32
+ *   dAqk, dAkk  [B, T, H, 64]   fp32; row = token, column = source index inside the
+ *                               token's chunk.  Entries outside the support (dAqk
+ *                               above the diagonal, dAkk on or above it) are ignored.
+ *   dq, dk, dg  [B, T, H, 128]  fp32 outputs, fully overwritten
+ *   db          [B, T, H]       fp32 output, fully overwritten
+ *
+ * Calls are asynchronous on `stream` (0 = the legacy default stream): no host
+ * synchronisation and no device allocation happens inside.  Inputs are not modified.
+ * Argument errors are reported before anything is launched; no call aborts the
+ * process.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_ABI_VERSION 1
+#define KDA_BT 64  /* chunk length */
+#define KDA_BC 16  /* sub-block length inside a chunk */
+#define KDA_K 128  /* head dimension */
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_NULL = 1,               /* a required pointer is NULL */
+    KDA_ERR_SHAPE = 2,              /* B, T or H <= 0, T % 64 != 0, or too large */
+    KDA_ERR_DTYPE = 3,              /* qk_dtype not KDA_BF16 / KDA_FP16 */
+    KDA_ERR_ALIGN = 4,              /* a pointer is not 16-byte aligned */
+    KDA_ERR_CUDA = 5,               /* a CUDA runtime call or the launch failed */
+    KDA_ERR_UNSUPPORTED_DEVICE = 6, /* current device is not compute capability 10.3 */
+    KDA_ERR_OVERLAP = 7,            /* two argument buffers overlap */
+    KDA_ERR_WORKSPACE = 8           /* workspace missing or too small (*_host only) */
+} kda_status_t;
+
+typedef enum { KDA_BF16 = 0, KDA_FP16 = 1 } kda_dtype_t;
+
+/*
+ * The intra-chunk backward, fast path: 16x16 diagonal sub-blocks on the FP32 pipes
+ * with one exp2 per (r, s, d); the cross-sub-block sums factorized through each
+ * sub-block's boundary gate (every exp2 argument <= 0) and contracted on the
+ * tensor cores in TF32 with FP32 accumulation.  Accuracy: max|err| / max|ref|
+ * <= 2e-3 per output tensor against the fp64 definition.
+ */
+kda_status_t kda_intra_bwd(const void *q, const void *k, const float *g,
+                           const float *beta, const float *dAqk, const float *dAkk,
+                           float *dq, float *dk, float *db, float *dg,
+                           int B, int T, int H, kda_dtype_t qk_dtype,
+                           kda_stream_t stream);
+
+/*
+ * Same contract, every product and sum in FP32 (the cross-sub-block sums on the
+ * FP32 pipes through the same boundary factorization).  Slower; accuracy
+ * max|err| / max|ref| <= 1e-4 per output tensor.
+ */
+kda_status_t kda_intra_bwd_fp32(const void *q, const void *k, const float *g,
+                                const float *beta, const float *dAqk, const float *dAkk,
+                                float *dq, float *dk, float *db, float *dg,
+                                int B, int T, int H, kda_dtype_t qk_dtype,
+                                kda_stream_t stream);
+
+/*
+ * End-to-end convenience for callers holding HOST buffers: copies the six inputs
+ * into `workspace` (device memory of at least kda_intra_bwd_host_workspace_bytes()
+ * bytes, caller-owned, 256-byte aligned), runs kda_intra_bwd on `stream`, and copies
+ * the four outputs back into the host buffers.  One cudaMemcpyAsync per tensor; the
+ * copies are truly asynchronous only when the host buffers are page-locked.  The
+ * call returns once everything is queued: synchronise `stream` before reading the
+ * outputs or reusing the inputs.  Host pointers need no particular alignment.
+ */
+size_t kda_intra_bwd_host_workspace_bytes(int B, int T, int H, kda_dtype_t qk_dtype);
+
+kda_status_t kda_intra_bwd_host(const void *q, const void *k, const float *g,
+                                const float *beta, const float *dAqk, const float *dAkk,
+                                float *dq, float *dk, float *db, float *dg,
+                                int B, int T, int H, kda_dtype_t qk_dtype,
+                                void *workspace, size_t workspace_bytes,
+                                kda_stream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *kda_status_str(kda_status_t status);
+
+/* KDA_ABI_VERSION of the loaded library. */
+int kda_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -28,3 +28,17 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _built_library():
+    """Build libkda.so in-tree if it is missing or older than its sources."""
+    import glob
+
+    from gated_delta_rule_intra_gb300 import build
+    srcs = glob.glob(os.path.join(build.CSRC, "*")) + glob.glob(
+        os.path.join(ROOT, "include", "*.h"))
+    if (not os.path.exists(build.LIB)
+            or os.path.getmtime(build.LIB) < max(os.path.getmtime(s) for s in srcs)):
+        build.build_library()
+    yield

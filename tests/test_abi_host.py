@@ -1,0 +1,142 @@
+"""libkda loads, exports what include/kda.h declares, and rejects bad arguments
+before touching the GPU (these tests never reach a CUDA call)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_delta_rule_intra_gb300 as kda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+(OK, ERR_NULL, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_CUDA, ERR_DEVICE, ERR_OVERLAP,
+ ERR_WORKSPACE) = range(9)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return kda.load_library()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("kda_intra_bwd", "kda_intra_bwd_fp32", "kda_intra_bwd_host",
+                 "kda_intra_bwd_host_workspace_bytes", "kda_status_str",
+                 "kda_abi_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libkda.so does not export {name}"
+
+
+def test_abi_version(lib):
+    text = open(HEADER).read()
+    want = int(re.search(r"#define KDA_ABI_VERSION (\d+)", text).group(1))
+    assert kda.kda_abi_version() == want
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        s = kda.kda_status_str(code)
+        assert s.startswith("KDA_")
+    assert kda.kda_status_str(99) == "KDA_ERR_UNKNOWN"
+
+
+# Fake, never-dereferenced device addresses: validation must fail first.
+BASE = 1 << 40
+SPAN = 1 << 34
+
+
+def fake_args(B=1, T=64, H=1, dtype=0, **override):
+    ptrs = {n: BASE + i * SPAN for i, n in enumerate(
+        ("q", "k", "g", "beta", "dAqk", "dAkk", "dq", "dk", "db", "dg"))}
+    ptrs.update(override)
+    vp = ctypes.c_void_p
+    return [vp(ptrs[n]) for n in ("q", "k", "g", "beta", "dAqk", "dAkk", "dq", "dk", "db",
+                                  "dg")] + [B, T, H, dtype, vp(0)]
+
+
+@pytest.mark.parametrize("fn", ["kda_intra_bwd", "kda_intra_bwd_fp32"])
+@pytest.mark.parametrize("case,want", [
+    (dict(q=0), ERR_NULL),
+    (dict(dg=0), ERR_NULL),
+    (dict(beta=0), ERR_NULL),
+    (dict(T=63), ERR_SHAPE),
+    (dict(T=100), ERR_SHAPE),
+    (dict(T=0), ERR_SHAPE),
+    (dict(B=0), ERR_SHAPE),
+    (dict(H=-1), ERR_SHAPE),
+    (dict(B=1 << 20, T=1 << 20, H=64), ERR_SHAPE),
+    (dict(dtype=2), ERR_DTYPE),
+    (dict(dtype=-1), ERR_DTYPE),
+    (dict(q=BASE + 8), ERR_ALIGN),
+    (dict(dAkk=BASE + 5 * SPAN + 4), ERR_ALIGN),
+    (dict(dq=BASE + 6 * SPAN + 2), ERR_ALIGN),
+    (dict(beta=BASE + 3 * SPAN + 2), ERR_ALIGN),
+    (dict(dq=BASE), ERR_OVERLAP),                 # output aliases q
+    (dict(dk=BASE + 6 * SPAN + 1024), ERR_OVERLAP),  # dk inside dq
+    (dict(db=BASE + 9 * SPAN + 16), ERR_OVERLAP),    # db inside dg
+])
+def test_rejected_before_launch(lib, fn, case, want):
+    case = dict(case)
+    shape = {k: case.pop(k) for k in ("B", "T", "H", "dtype") if k in case}
+    rc = getattr(lib, fn)(*fake_args(**shape, **case))
+    assert rc == want, kda.kda_status_str(rc)
+
+
+def test_inputs_may_alias_each_other(lib):
+    # q == k is a legal call (read-only inputs); it must get past validation.  With
+    # no GPU in this process the call then stops at the device query, never earlier.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("would launch on a real device")
+    rc = lib.kda_intra_bwd(*fake_args(k=BASE))
+    assert rc in (ERR_CUDA, ERR_DEVICE)
+
+
+def test_host_entry_point_validation(lib):
+    vp = ctypes.c_void_p
+    args = fake_args()[:-1]
+    need = lib.kda_intra_bwd_host_workspace_bytes(1, 64, 1, 0)
+    assert need > 0
+    assert lib.kda_intra_bwd_host(*args, vp(0), need, vp(0)) == ERR_WORKSPACE
+    assert lib.kda_intra_bwd_host(*args, vp(BASE + 20 * SPAN), need - 1, vp(0)) == ERR_WORKSPACE
+    assert lib.kda_intra_bwd_host(*args, vp(BASE + 20 * SPAN + 16), need, vp(0)) == ERR_ALIGN
+    bad = fake_args(T=65)[:-1]
+    assert lib.kda_intra_bwd_host(*bad, vp(BASE + 20 * SPAN), need, vp(0)) == ERR_SHAPE
+    assert lib.kda_intra_bwd_host_workspace_bytes(1, 65, 1, 0) == 0
+    assert lib.kda_intra_bwd_host_workspace_bytes(1, 64, 1, 7) == 0
+
+
+def test_workspace_size_formula(lib):
+    B, T, H = 2, 128, 3
+    rows = B * T * H
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    want = 2 * al(rows * 256) + 4 * al(rows * 512) + 2 * al(rows * 4) + 2 * al(rows * 256)
+    assert lib.kda_intra_bwd_host_workspace_bytes(B, T, H, 0) == want
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 64, 1, 128, dtype=torch.bfloat16)
+    f = torch.zeros(1, 64, 1, 128)
+    b = torch.zeros(1, 64, 1)
+    a = torch.zeros(1, 64, 1, 64)
+    with pytest.raises(ValueError, match="CUDA"):
+        kda.kda_intra_bwd(q, q, f, b, a, a)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="no fallback"):
+        kda.load_library(str(tmp_path / "libkda.so"))

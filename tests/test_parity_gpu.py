@@ -1,0 +1,182 @@
+"""CUDA path against the fp64 oracle, element by element, through the C ABI."""
+
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_intra_gb300 as kda
+import kda_inputs
+from tests import _gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def config_inputs():
+    cache = {}
+
+    def get(idx):
+        if idx not in cache:
+            cpu = kda_inputs.make_config_inputs(idx)
+            cache.clear()  # keep at most one large config resident
+            cache[idx] = (cpu, _gpu.to_device(cpu))
+        return cache[idx]
+    yield get
+    cache.clear()
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("path", _gpu.PATHS)
+@pytest.mark.parametrize("cfg", [0, 1])
+def test_full_parity_small_configs(config_inputs, path, cfg):
+    cpu, dev = config_inputs(cfg)
+    got = _gpu.run(path, dev)
+    torch.cuda.synchronize()
+    ref = _gpu.oracle_outputs(cpu)
+    _gpu.assert_close(got, ref, _gpu.TOL[path], f"{path} config {cfg}")
+
+
+@pytest.mark.parametrize("path", _gpu.PATHS)
+@pytest.mark.parametrize("cfg", [2, 3, 4])
+def test_full_parity_full_size(config_inputs, path, cfg):
+    """Full-size launch (the benchmark's configuration), every element vs the oracle."""
+    cpu, dev = config_inputs(cfg)
+    outs = _gpu.run(path, dev)
+    torch.cuda.synchronize()
+    ref = _gpu.oracle_outputs(cpu)
+    _gpu.assert_close(outs, ref, _gpu.TOL[path], f"{path} config {cfg}")
+    del ref
+    # properties that hold at any size, checked on every unit of the launch
+    cf = kda_inputs.CONFIGS[cfg]
+    for x in outs:
+        assert torch.isfinite(x).all()
+    dg = outs[3].view(cf.B, cf.T // 64, 64, cf.H, 128)
+    colsum = dg.sum(dim=2).abs().max().item()
+    assert colsum <= 1e-4 * dg.abs().max().item() * 8, "sum_t dg over a chunk != 0"
+
+
+@pytest.mark.parametrize("path", _gpu.PATHS)
+@pytest.mark.parametrize("shape", [(1, 64, 1), (3, 192, 5), (1, 128, 7), (2, 64, 3)])
+def test_odd_shapes(path, shape):
+    B, T, H = shape
+    cpu = kda_inputs.make_inputs(B, T, H, seed=B * 1000 + T + H)
+    got = _gpu.run(path, _gpu.to_device(cpu))
+    _gpu.assert_close(got, _gpu.oracle_outputs(cpu), _gpu.TOL[path], f"{path} {shape}")
+
+
+@pytest.mark.parametrize("path", _gpu.PATHS)
+def test_fp16_gate_stress_small(path):
+    cpu = kda_inputs.make_inputs(2, 256, 3, gate_lo=-8.0, qk_dtype=torch.float16, seed=4)
+    got = _gpu.run(path, _gpu.to_device(cpu))
+    _gpu.assert_close(got, _gpu.oracle_outputs(cpu), _gpu.TOL[path], f"{path} stress")
+
+
+@pytest.mark.parametrize("path", _gpu.PATHS)
+def test_out_of_support_entries_are_ignored(path):
+    """Poison dAqk above the diagonal and dAkk on/above it: bitwise same outputs."""
+    cpu = kda_inputs.make_inputs(2, 128, 2, seed=11)
+    dev = _gpu.to_device(cpu)
+    base = _gpu.run(path, dev)
+    lower, strict = kda_inputs.chunk_masks()
+    up_q = (~lower).repeat(2, 1).view(1, 128, 1, 64).cuda()
+    up_k = (~strict).repeat(2, 1).view(1, 128, 1, 64).cuda()
+    dev["dAqk"] = torch.where(up_q, torch.full_like(dev["dAqk"], 3e38), dev["dAqk"])
+    dev["dAkk"] = torch.where(up_k, torch.full_like(dev["dAkk"], float("nan")), dev["dAkk"])
+    got = _gpu.run(path, dev)
+    for n, a, b in zip(_gpu.NAMES, got, base):
+        assert torch.equal(a, b), f"{n} depends on out-of-support dA entries"
+
+
+@pytest.mark.parametrize("path", _gpu.PATHS)
+def test_every_output_written_and_nothing_else(path):
+    """NaN-prefilled outputs inside canary-padded buffers."""
+    B, T, H = 2, 192, 3
+    cpu = kda_inputs.make_inputs(B, T, H, seed=12)
+    dev = _gpu.to_device(cpu)
+    pad = 4096
+    outs = []
+    for shape in ((B, T, H, 128), (B, T, H, 128), (B, T, H), (B, T, H, 128)):
+        n = int(np.prod(shape))
+        buf = torch.full((n + 2 * pad,), float("nan"), device="cuda")
+        buf[:pad] = 1234.5
+        buf[-pad:] = -4321.5
+        outs.append((buf, buf[pad:pad + n].view(shape)))
+    dq, dk, db, dg = (o[1] for o in outs)
+    _gpu.run(path, dev, dq=dq, dk=dk, db=db, dg=dg)
+    torch.cuda.synchronize()
+    for buf, view in outs:
+        assert torch.isfinite(view).all()
+        assert (buf[:pad] == 1234.5).all() and (buf[-pad:] == -4321.5).all()
+    _gpu.assert_close((dq, dk, db, dg), _gpu.oracle_outputs(cpu), _gpu.TOL[path], path)
+
+
+@pytest.mark.parametrize("path", _gpu.PATHS)
+def test_deterministic(path):
+    cpu = kda_inputs.make_inputs(2, 256, 4, seed=13)
+    dev = _gpu.to_device(cpu)
+    a = _gpu.run(path, dev)
+    b = _gpu.run(path, dev)
+    for n, x, y in zip(_gpu.NAMES, a, b):
+        assert torch.equal(x, y), f"{n} differs between identical calls"
+
+
+@pytest.mark.parametrize("path", _gpu.PATHS)
+def test_zero_gradients_give_zero_outputs(path):
+    cpu = kda_inputs.make_inputs(1, 128, 2, seed=14)
+    cpu["dAqk"].zero_()
+    cpu["dAkk"].zero_()
+    got = _gpu.run(path, _gpu.to_device(cpu))
+    for n, x in zip(_gpu.NAMES, got):
+        assert torch.count_nonzero(x).item() == 0, n
+
+
+@pytest.mark.parametrize("path", _gpu.PATHS)
+def test_gate_free(path):
+    cpu = kda_inputs.make_inputs(1, 128, 2, seed=15)
+    cpu["g"].zero_()
+    got = _gpu.run(path, _gpu.to_device(cpu))
+    _gpu.assert_close(got, _gpu.oracle_outputs(cpu), _gpu.TOL[path], f"{path} g=0")
+
+
+def test_side_stream_and_paths_agree():
+    cpu = kda_inputs.make_inputs(2, 256, 2, seed=16)
+    dev = _gpu.to_device(cpu)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        got = _gpu.run("kda_intra_bwd", dev, stream=s)
+    s.synchronize()
+    ref = _gpu.run("kda_intra_bwd_fp32", dev)
+    _gpu.assert_close(got, [x.cpu().double().numpy() for x in ref], 2e-3, "fast vs fp32")
+
+
+def test_host_entry_point_matches_device_path():
+    B, T, H = 2, 256, 3
+    cpu = kda_inputs.make_inputs(B, T, H, seed=17)
+    pinned = {n: v.pin_memory() for n, v in cpu.items()}
+    outs = [torch.empty(B, T, H, 128).pin_memory(), torch.empty(B, T, H, 128).pin_memory(),
+            torch.empty(B, T, H).pin_memory(), torch.empty(B, T, H, 128).pin_memory()]
+    nbytes = kda.kda_intra_bwd_host_workspace_bytes(B, T, H, torch.bfloat16)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    kda.kda_intra_bwd_host(*(pinned[n] for n in _gpu.ARGS), *outs, workspace=ws)
+    torch.cuda.current_stream().synchronize()
+    ref = _gpu.run("kda_intra_bwd", _gpu.to_device(cpu))
+    for n, a, b in zip(_gpu.NAMES, outs, ref):
+        assert torch.equal(a, b.cpu()), n
+
+
+def test_misaligned_pointer_is_a_status_not_a_fault():
+    cpu = kda_inputs.make_inputs(1, 64, 1, seed=18)
+    dev = _gpu.to_device(cpu)
+    buf = torch.empty(64 * 128 + 1, device="cuda")
+    bad = buf[1:].view(1, 64, 1, 128)  # 4 bytes off a 16-byte boundary
+    bad.copy_(dev["g"])
+    for path in _gpu.PATHS:
+        with pytest.raises(kda.KdaError, match="ALIGN"):
+            getattr(kda, path)(dev["q"], dev["k"], bad, dev["beta"], dev["dAqk"], dev["dAkk"])
+
+
+def test_sampled_units_match_full_launch():
+    """The sampled-unit helper the benchmark uses agrees with the full launch."""
+    cpu = kda_inputs.make_config_inputs(1)
+    dev = _gpu.to_device(cpu)
+    _gpu.sampled_parity("kda_intra_bwd", 1, cpu, dev, n_units=8)
