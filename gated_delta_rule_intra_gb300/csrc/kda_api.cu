@@ -4,7 +4,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/kda.h"
+#include "kda.h"
 #include "kda_launch.h"
 
 namespace {
@@ -21,7 +21,7 @@ struct Range {
 bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
 kda_status_t check_shape(int B, int T, int H) {
-    if (B <= 0 || T <= 0 || H <= 0) return KDA_ERR_SHAPE;
+    if (B <= 0 || T <= 0 || H <= 0 || H > KDA_MAX_H) return KDA_ERR_SHAPE;
     if (T % KDA_BT != 0) return KDA_ERR_SHAPE;
     const long long rows = (long long)B * T * H;
     const long long units = rows / KDA_BT;
@@ -192,7 +192,8 @@ const char *kda_status_str(kda_status_t status) {
     switch (status) {
         case KDA_OK: return "KDA_OK";
         case KDA_ERR_NULL: return "KDA_ERR_NULL: a required pointer is NULL";
-        case KDA_ERR_SHAPE: return "KDA_ERR_SHAPE: need B,T,H > 0 and T % 64 == 0";
+        case KDA_ERR_SHAPE:
+            return "KDA_ERR_SHAPE: need B,T > 0, 0 < H <= 65536 and T % 64 == 0";
         case KDA_ERR_DTYPE: return "KDA_ERR_DTYPE: qk_dtype must be KDA_BF16 or KDA_FP16";
         case KDA_ERR_ALIGN: return "KDA_ERR_ALIGN: a pointer is misaligned";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA call or kernel launch failed";

@@ -62,6 +62,7 @@ extern "C" {
 #define KDA_BT 64  /* chunk length */
 #define KDA_BC 16  /* sub-block length inside a chunk */
 #define KDA_K 128  /* head dimension */
+#define KDA_MAX_H 65536 /* largest supported head count */
 
 /* Same type as cudaStream_t, declared without the CUDA headers. */
 typedef struct CUstream_st *kda_stream_t;
@@ -69,7 +70,7 @@ typedef struct CUstream_st *kda_stream_t;
 typedef enum {
     KDA_OK = 0,
     KDA_ERR_NULL = 1,               /* a required pointer is NULL */
-    KDA_ERR_SHAPE = 2,              /* B, T or H <= 0, T % 64 != 0, or too large */
+    KDA_ERR_SHAPE = 2,              /* B,T,H <= 0, H > KDA_MAX_H, T % 64 != 0, too large */
     KDA_ERR_DTYPE = 3,              /* qk_dtype not KDA_BF16 / KDA_FP16 */
     KDA_ERR_ALIGN = 4,              /* a pointer is not 16-byte aligned */
     KDA_ERR_CUDA = 5,               /* a CUDA runtime call or the launch failed */
