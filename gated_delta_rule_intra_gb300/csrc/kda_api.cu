@@ -26,6 +26,7 @@ kda_status_t check_shape(int B, int T, int H) {
     const long long rows = (long long)B * T * H;
     const long long units = rows / KDA_BT;
     if (units > 0x7fffffffLL) return KDA_ERR_SHAPE;     // grid limit
+    if ((long long)B * T > 0x7fffffffLL) return KDA_ERR_SHAPE;  // 32-bit TMA row coordinate
     if (rows > (1LL << 52) / KDA_K) return KDA_ERR_SHAPE; // index arithmetic headroom
     return KDA_OK;
 }

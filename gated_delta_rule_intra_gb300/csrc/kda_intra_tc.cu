@@ -1,8 +1,18 @@
-// Tensor-core kernel for the KDA intra-chunk backward (sm_103a, tcgen05 + TMEM).
+// Tensor-core kernel for the KDA intra-chunk backward (sm_103a, tcgen05 + TMEM + TMA).
 //
-// Persistent grid (one 512-thread CTA per SM), units (b, h, 64-token chunk) dealt
-// round-robin.  Each unit's inputs are staged with 16-byte cp.async into one of two
-// shared-memory stages while the previous unit is being computed.
+// Persistent grid, one 512-thread CTA per SM, units (b, h, 64-token chunk) dealt
+// round-robin.  Two shared-memory stages hold the inputs of consecutive units; the
+// tensor memory accelerator fills a stage while the other one is being computed.
+// There is no CTA-wide barrier inside the unit loop: warps hand work to each other
+// through mbarriers and two shared counters, so fast warps run ahead into the
+// next unit instead of idling:
+//   * the stage-full mbarrier completes when a unit's TMA tiles and beta have landed;
+//   * the last warp to finish writing its tensor-core operands issues the unit's 36
+//     MMAs (every other warp goes straight on to the diagonal blocks);
+//   * the last warp to finish a unit releases its stage and loads the unit after
+//     next into it;
+//   * the per-row sum for dbeta meets across the four warps of a sub-block at a
+//     128-thread named barrier.
 //
 // Thread (i, d) owns sub-block i (rows 16i..16i+15) at channel d; its TMEM lane is d
 // (warp w reaches lanes 32(w%4)..32(w%4)+31, and d = 32(w%4) + lane).
@@ -20,8 +30,11 @@
 //     P_j[d, s] = sum_{r in blk j} q[r,d] 2^(g_r - g_16j) dAqk[r,s]
 //               + beta_r k[r,d] 2^(g_r - g_16j) dAkk[r,s]        (s < 16j)
 //     dkt_cross[s,d] = 2^(g_e(i) - g_s) * sum_{j>i} 2^(g_16j - g_e(i)) P_j[d, s].
-// 36 MMAs (M=128 channels, N=16..48, K=8) per unit, issued by one thread, run while
-// all warps compute the 16x16 diagonal blocks with one exp2 per (r, s, d).
+// The 16x16 diagonal blocks run on the FP32 pipes with one exp2 per (r, s, d),
+// two source rows at a time in packed FP32x2 arithmetic.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "kda_common.cuh"
 #include "kda_launch.h"
 #include "tc_ptx.cuh"
@@ -30,27 +43,40 @@ namespace kda {
 namespace {
 
 constexpr int TC_THREADS = 512;
+constexpr int TC_WARPS = TC_THREADS / 32;
 
 // ---- shared memory: two input stages + single-buffered derived operands ----
-constexpr int ST_Q = 0;                        // io_t [64][128]
-constexpr int ST_K = ST_Q + BT * KD * 2;       // io_t [64][128]
-constexpr int ST_G = ST_K + BT * KD * 2;       // f32  [64][128]
-constexpr int ST_BQ = ST_G + BT * KD * 4;      // dAqk rows of block t, cols < 16t (K-major core layout)
-constexpr int ST_BK = ST_BQ + 6144;            // same for dAkk
-constexpr int ST_DQ = ST_BK + 6144;            // dAqk diagonal blocks f32 [4][16][16]
-constexpr int ST_DK = ST_DQ + 4096;            // dAkk diagonal blocks
-constexpr int ST_BETA = ST_DK + 4096;          // f32 [64]
-constexpr int STAGE_BYTES = ST_BETA + 256;     // 86272
-constexpr int SM_BCQ = 2 * STAGE_BYTES;        // dAqk blocks of target j transposed (K-major)
+// dA tiles: the ten lower 16x16 blocks (t, j <= t) of a unit, block (t, j) at
+// dablk(t, j) KB, each in the K-major core-matrix layout of a tensor-core operand:
+// element (n, k) (n = row in block t, k = column in block j) at byte
+//     (k/4)*256 + (n/8)*128 + (n%8)*16 + (k%4)*4.
+// Blocks (t, 0..t-1) are contiguous, so they form the B operand of target t
+// (N = 16 rows, K = 16t, core matrices 256 B apart along K and 128 B along N).
+constexpr int ST_Q = 0;                      // io_t [64][128]
+constexpr int ST_K = ST_Q + BT * KD * 2;     // io_t [64][128]
+constexpr int ST_G = ST_K + BT * KD * 2;     // f32  [64][128]
+constexpr int ST_DQ = ST_G + BT * KD * 4;    // dAqk: 10 blocks x 1 KB
+constexpr int ST_DK = ST_DQ + 10 * 1024;     // dAkk
+constexpr int ST_BETA = ST_DK + 10 * 1024;   // f32 [64]
+constexpr int STAGE_BYTES = ST_BETA + 256;   // 86272
+constexpr int SM_BCQ = 2 * STAGE_BYTES;      // dAqk blocks of target j transposed (K-major)
 constexpr int SM_BCK = SM_BCQ + 6144;
-constexpr int SM_DBP = SM_BCK + 6144;          // db partials f32 [4][64]
-constexpr int SM_MBAR = SM_DBP + 1024;
-constexpr int SM_TSLOT = SM_MBAR + 16;
+constexpr int SM_DBP = SM_BCK + 6144;        // db partials f32 [4][64]
+constexpr int SM_FULL = SM_DBP + 1024;       // 2 stage-full mbarriers
+constexpr int SM_MMA = SM_FULL + 16;         // MMAs-done mbarrier
+constexpr int SM_CNT = SM_MMA + 8;           // operand counter, unit-done counter
+constexpr int SM_TSLOT = SM_CNT + 8;
 constexpr int SM_TOTAL = SM_TSLOT + 8;
-static_assert(STAGE_BYTES % 128 == 0, "stage alignment");
+static_assert(STAGE_BYTES % 128 == 0, "TMA destinations need 128-byte alignment");
+static_assert(ST_DQ % 1024 == 0 && ST_DK % 1024 == 0, "dA tiles alignment");
 
-// byte offset of block t's operand inside a 6 KB B region: sizes 1, 2, 3 KB
-__device__ __forceinline__ uint32_t blk_off(int t) { return 512u * (uint32_t)((t - 1) * t); }
+constexpr uint32_t STAGE_TX_BYTES = 2 * BT * KD * 2 + BT * KD * 4 + 2 * 10 * 1024;
+constexpr uint32_t FULL_ARRIVALS = 1 + 32;  // expect_tx by lane 0 + beta copies by 32 lanes
+
+__host__ __device__ constexpr int dablk(int t, int j) { return t * (t + 1) / 2 + j; }
+
+// byte offset of target j's transposed operand inside a 6 KB region: 1, 2, 3 KB
+__device__ __forceinline__ uint32_t bcol_off(int j) { return 512u * (uint32_t)((j - 1) * j); }
 
 // ---- TMEM column map (512 columns, fp32) ----
 __device__ __forceinline__ uint32_t tm_arow(int t) { return 8u * (uint32_t)(t * (t - 1)); }  // A_t: 16t cols
@@ -63,66 +89,54 @@ constexpr uint32_t TM_FB = 384;    // 2^(g_r - g_16i) for block i >= 1 at +16(i-
 constexpr uint32_t TM_FA = 432;    // 2^(g_16(i+1) - g_s) for block i <= 2 at +16i
 constexpr uint32_t TM_COLS = 512;
 
-constexpr uint32_t MBAR_SPIN_LIMIT = 1u << 20;
+constexpr uint32_t SPIN_LIMIT = 1u << 22;
+
+struct TmaMaps {
+    CUtensorMap q, k, g, daqk, dakk;
+};
 
 __device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
     uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(gmem) : "memory");
 }
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
-// Queue this thread's share of one unit's input copies into a stage.  Row r of
-// the unit sits at global row `row0 + r*H` of every [B, T, H, *] tensor.
-template <typename io_t>
-__device__ __forceinline__ void issue_unit_loads(unsigned char *st, const io_t *__restrict__ q,
-                                                 const io_t *__restrict__ k,
-                                                 const float *__restrict__ g,
-                                                 const float *__restrict__ beta,
-                                                 const float *__restrict__ dAqk,
-                                                 const float *__restrict__ dAkk,
-                                                 size_t row0, int H, int tid) {
-    const size_t e128 = row0 * KD, e64 = row0 * BT;
-    const uint32_t hk = (uint32_t)H * KD;
+// One warp queues every copy of one unit into a stage: 23 TMA tiles from lane 0,
+// beta as 64 four-byte copies from all lanes (its rows are H floats apart, so no
+// tensor map can describe it when H is not a multiple of 4).
+__device__ __forceinline__ void load_unit(unsigned char *st, uint64_t *full,
+                                          const TmaMaps &tm, const float *__restrict__ beta,
+                                          long long u, int T, int H, int lane) {
+    const Unit x = decode_unit(u, H, T / BT);
+    const int row = x.b * T + x.c * BT;  // first token row of the unit
+    if (lane == 0) {
+        tc::mbar_arrive_expect_tx(full, STAGE_TX_BYTES);
+        tc::tma_load_3d(st + ST_Q, &tm.q, 0, x.h, row, full);
+        tc::tma_load_3d(st + ST_K, &tm.k, 0, x.h, row, full);
+        tc::tma_load_3d(st + ST_G, &tm.g, 0, x.h, row, full);
 #pragma unroll
-    for (int x = 0; x < 2; ++x) {  // q, k: 64 rows x 16 chunks
-        const int r = (tid >> 4) + 32 * x, c = tid & 15;
-        const size_t off = e128 + (size_t)((uint32_t)r * hk + c * 8);
-        cp_async16(st + ST_Q + r * 256 + c * 16, q + off);
-        cp_async16(st + ST_K + r * 256 + c * 16, k + off);
-    }
+        for (int t = 0; t < NBLK; ++t) {
 #pragma unroll
-    for (int x = 0; x < 4; ++x) {  // g: 64 rows x 32 chunks
-        const int r = (tid >> 5) + 16 * x, c = tid & 31;
-        cp_async16(st + ST_G + r * 512 + c * 16, g + e128 + (size_t)((uint32_t)r * hk + c * 4));
-    }
-    // dA: 64 rows x 16 chunks, of which row r of block t needs the first 4(t+1):
-    // 4t off-diagonal chunks for the tensor-core operand of block t, then the
-    // 4 chunks of the diagonal block.
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
-        const int r = (tid >> 4) + 32 * x, c = tid & 15;
-        const int t = r >> 4, n = r & 15;
-        if (c < 4 * (t + 1)) {
-            const size_t src = e64 + (size_t)((uint32_t)r * H * BT + c * 4);
-            const bool off_diag = c < 4 * t;
-            const uint32_t dst =
-                off_diag ? blk_off(t) + (uint32_t)((n >> 3) * (512 * t) + c * 128 + (n & 7) * 16)
-                         : (uint32_t)(t * 1024 + n * 64 + (c - 4 * t) * 16);
-            cp_async16(st + (off_diag ? ST_BQ : ST_DQ) + dst, dAqk + src);
-            cp_async16(st + (off_diag ? ST_BK : ST_DK) + dst, dAkk + src);
+            for (int j = 0; j <= t; ++j) {
+                const int rg = (row + BC * t) >> 3;
+                tc::tma_load_5d(st + ST_DQ + dablk(t, j) * 1024, &tm.daqk, 0, 0, rg, 4 * j, x.h,
+                                full);
+                tc::tma_load_5d(st + ST_DK + dablk(t, j) * 1024, &tm.dakk, 0, 0, rg, 4 * j, x.h,
+                                full);
+            }
         }
     }
-    if (tid < BT) cp_async4(st + ST_BETA + tid * 4, beta + row0 + (size_t)tid * H);
+    const size_t b0 = grow(x, 0, T, H);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int r = lane + 32 * e;
+        cp_async4(st + ST_BETA + r * 4, beta + b0 + (size_t)r * H);
+    }
+    tc::cp_async_mbar_arrive_noinc(full);
 }
 
 template <typename io_t>
 __global__ void __launch_bounds__(TC_THREADS, 1)
-kda_intra_bwd_tc_kernel(const io_t *__restrict__ q, const io_t *__restrict__ k,
-                        const float *__restrict__ g, const float *__restrict__ beta,
-                        const float *__restrict__ dAqk, const float *__restrict__ dAkk,
+kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restrict__ beta,
                         float *__restrict__ dq, float *__restrict__ dk,
                         float *__restrict__ db, float *__restrict__ dg, int T, int H,
                         long long units) {
@@ -133,15 +147,26 @@ kda_intra_bwd_tc_kernel(const io_t *__restrict__ q, const io_t *__restrict__ k,
     const int d = tid & 127;
     const int r0 = i * BC;
     const int NT = T / BT;
-    uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + SM_MBAR);          // MMAs done
-    uint32_t *ops_count = reinterpret_cast<uint32_t *>(smem + SM_MBAR + 8);  // warps done
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM_FULL);
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + SM_MMA);
+    uint32_t *ops_count = reinterpret_cast<uint32_t *>(smem + SM_CNT);
+    uint32_t *done_count = ops_count + 1;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + SM_TSLOT);
     float *sdbp = reinterpret_cast<float *>(smem + SM_DBP);
+    const long long stride = gridDim.x;
 
     if (warp == 0) tc::tmem_alloc(tslot, TM_COLS);
     if (tid == 0) {
+        tc::mbar_init(&full[0], FULL_ARRIVALS);
+        tc::mbar_init(&full[1], FULL_ARRIVALS);
         tc::mbar_init(mbar, 1);
-        *ops_count = 0u;
+        ops_count[0] = 0u;
+        done_count[0] = 0u;
+        tc::prefetch_tmap(&tm.q);
+        tc::prefetch_tmap(&tm.k);
+        tc::prefetch_tmap(&tm.g);
+        tc::prefetch_tmap(&tm.daqk);
+        tc::prefetch_tmap(&tm.dakk);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -149,22 +174,19 @@ kda_intra_bwd_tc_kernel(const io_t *__restrict__ q, const io_t *__restrict__ k,
     const uint32_t tbase = *tslot;
     const uint32_t tlane = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
 
-    long long u = blockIdx.x;
-    if (u < units)
-        issue_unit_loads(smem, q, k, g, beta, dAqk, dAkk, grow(decode_unit(u, H, NT), 0, T, H), H,
-                         tid);
-    cp_async_commit();
+    if (warp == 0) {  // the first two units of this CTA
+        const long long u0 = blockIdx.x;
+        if (u0 < units) load_unit(smem, &full[0], tm, beta, u0, T, H, lane);
+        if (u0 + stride < units)
+            load_unit(smem + STAGE_BYTES, &full[1], tm, beta, u0 + stride, T, H, lane);
+    }
 
-    uint32_t phase = 0;
-    for (int it = 0; u < units; ++it, u += gridDim.x) {
-        unsigned char *st = smem + (it & 1) * STAGE_BYTES;
-        const Unit un = decode_unit(u, H, NT);
-        if (u + gridDim.x < units)
-            issue_unit_loads(smem + ((it + 1) & 1) * STAGE_BYTES, q, k, g, beta, dAqk, dAkk,
-                             grow(decode_unit(u + gridDim.x, H, NT), 0, T, H), H, tid);
-        cp_async_commit();
-        cp_async_wait_group<1>();
-        __syncthreads();
+    bool ok = true;
+    int it = 0;
+    for (long long u = blockIdx.x; u < units; u += stride, ++it) {
+        const int sidx = it & 1;
+        unsigned char *st = smem + sidx * STAGE_BYTES;
+        ok &= tc::mbar_wait(&full[sidx], (uint32_t)(it >> 1) & 1u, SPIN_LIMIT);
 
         const float *sg = reinterpret_cast<const float *>(st + ST_G);
         const io_t *sq = reinterpret_cast<const io_t *>(st + ST_Q);
@@ -220,10 +242,10 @@ kda_intra_bwd_tc_kernel(const io_t *__restrict__ q, const io_t *__restrict__ k,
             tc::tmem_st16(tlane + TM_AKBB + 16 * (i - 1), v);
         }
 
-        // ---- column-side B operands: dA blocks of target j transposed ----
+        // ---- column-side B operands: dA blocks (j, 0..j-1) transposed ----
         {
-            const float *bq = reinterpret_cast<const float *>(st + ST_BQ);
-            const float *bk = reinterpret_cast<const float *>(st + ST_BK);
+            const float *aq = reinterpret_cast<const float *>(st + ST_DQ);
+            const float *ak = reinterpret_cast<const float *>(st + ST_DK);
             float *cq = reinterpret_cast<float *>(smem + SM_BCQ);
             float *ck = reinterpret_cast<float *>(smem + SM_BCK);
 #pragma unroll
@@ -231,18 +253,19 @@ kda_intra_bwd_tc_kernel(const io_t *__restrict__ q, const io_t *__restrict__ k,
                 const int idx = tid + x * TC_THREADS;  // < 1536
                 const int j = idx >= 768 ? 3 : idx >= 256 ? 2 : 1;
                 const int e = idx - 128 * j * (j - 1);
-                // e enumerates the destination bytes/4 in order: (n/8, k/4, n%8, k%4)
+                // e enumerates the destination floats in order (n/8, k/4, n%8, k%4)
                 const int n = (e >> 7) * 8 + ((e >> 2) & 7);  // s
                 const int kk = ((e >> 5) & 3) * 4 + (e & 3);  // r - 16j
-                const int src = (int)blk_off(j) / 4 + (kk >> 3) * (128 * j) + (n >> 2) * 32 +
+                const int src = dablk(j, n >> 4) * 256 + ((n & 15) >> 2) * 64 + (kk >> 3) * 32 +
                                 (kk & 7) * 4 + (n & 3);
-                const int dst = (int)blk_off(j) / 4 + e;
-                cq[dst] = bq[src];
-                ck[dst] = bk[src];
+                const int dst = (int)bcol_off(j) / 4 + e;
+                cq[dst] = aq[src];
+                ck[dst] = ak[src];
             }
         }
+
         // operands complete: TMEM stores landed, smem stores visible to the tensor core;
-        // the last warp to finish issues the 36 MMAs (no thread waits for the others)
+        // the last warp to get here issues the 36 MMAs (no thread waits for the others)
         tc::tmem_wait_st();
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
@@ -250,38 +273,40 @@ kda_intra_bwd_tc_kernel(const io_t *__restrict__ q, const io_t *__restrict__ k,
         uint32_t prev = 0;
         if (lane == 0) prev = tc::atomic_add_acq_rel_smem(ops_count, 1u);
         prev = __shfl_sync(0xffffffffu, prev, 0);
-        if ((prev & 15u) == 15u && lane == 0) {
+        // The branch is warp-uniform so the descriptor arithmetic stays on the uniform
+        // datapath; one elected lane issues.
+        if ((prev % TC_WARPS) == TC_WARPS - 1) {
             tc::fence_after_sync();
-            const uint32_t bq = tc::smem_u32(st + ST_BQ), bk = tc::smem_u32(st + ST_BK);
+            const uint64_t dq0 = tc::smem_desc(tc::smem_u32(st + ST_DQ), 256, 128);
+            const uint64_t dk0 = tc::smem_desc(tc::smem_u32(st + ST_DK), 256, 128);
+            const uint64_t cq0 = tc::smem_desc(tc::smem_u32(smem + SM_BCQ), 128, 512);
+            const uint64_t ck0 = tc::smem_desc(tc::smem_u32(smem + SM_BCK), 128, 512);
             const uint32_t id16 = tc::idesc_tf32(128, 16);
+            if (tc::elect_one()) {
 #pragma unroll
-            for (int t = 1; t < NBLK; ++t) {
+                for (int t = 1; t < NBLK; ++t) {
 #pragma unroll
-                for (int kk = 0; kk < 2 * t; ++kk) {
-                    const uint32_t a = tbase + tm_arow(t) + 8 * kk;
-                    const uint32_t boff = blk_off(t) + 256 * kk;
-                    tc::mma_tf32_ts(tbase + TM_XQ + 16 * (t - 1), a,
-                                    tc::smem_desc(bq + boff, 128, 512 * t), id16, kk > 0);
-                    tc::mma_tf32_ts(tbase + TM_XK + 16 * (t - 1), a,
-                                    tc::smem_desc(bk + boff, 128, 512 * t), id16, kk > 0);
+                    for (int kk = 0; kk < 2 * t; ++kk) {
+                        const uint32_t a = tbase + tm_arow(t) + 8 * kk;
+                        const uint64_t boff = (uint64_t)((dablk(t, 0) * 1024 + 512 * kk) >> 4);
+                        tc::mma_tf32_ts(tbase + TM_XQ + 16 * (t - 1), a, dq0 + boff, id16, kk > 0);
+                        tc::mma_tf32_ts(tbase + TM_XK + 16 * (t - 1), a, dk0 + boff, id16, kk > 0);
+                    }
                 }
+#pragma unroll
+                for (int j = 1; j < NBLK; ++j) {
+                    const uint32_t idj = tc::idesc_tf32(128, 16 * j);
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk)
+                        tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AQB + 16 * (j - 1) + 8 * kk,
+                                        cq0 + ((bcol_off(j) + 256 * kk) >> 4), idj, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk)
+                        tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AKBB + 16 * (j - 1) + 8 * kk,
+                                        ck0 + ((bcol_off(j) + 256 * kk) >> 4), idj, true);
+                }
+                tc::mma_commit(mbar);
             }
-            const uint32_t cq = tc::smem_u32(smem + SM_BCQ), ck = tc::smem_u32(smem + SM_BCK);
-#pragma unroll
-            for (int j = 1; j < NBLK; ++j) {
-                const uint32_t idj = tc::idesc_tf32(128, 16 * j);
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk)
-                    tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AQB + 16 * (j - 1) + 8 * kk,
-                                    tc::smem_desc(cq + blk_off(j) + 256 * kk, 128, 512), idj,
-                                    kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk)
-                    tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AKBB + 16 * (j - 1) + 8 * kk,
-                                    tc::smem_desc(ck + blk_off(j) + 256 * kk, 128, 512), idj,
-                                    true);
-            }
-            tc::mma_commit(mbar);
         }
         __syncwarp();
 
@@ -292,8 +317,8 @@ kda_intra_bwd_tc_kernel(const io_t *__restrict__ q, const io_t *__restrict__ k,
 #pragma unroll
         for (int m = 0; m < BC / 2; ++m) dkt2[m] = make_float2(0.f, 0.f);
         {
-            const float *dgq = reinterpret_cast<const float *>(st + ST_DQ) + i * 256;
-            const float *dgk = reinterpret_cast<const float *>(st + ST_DK) + i * 256;
+            const float *dgq = reinterpret_cast<const float *>(st + ST_DQ) + dablk(i, i) * 256;
+            const float *dgk = reinterpret_cast<const float *>(st + ST_DK) + dablk(i, i) * 256;
             const float2 neg1 = make_float2(-1.f, -1.f);
 #pragma unroll
             for (int r = 0; r < BC; ++r) {
@@ -304,12 +329,14 @@ kda_intra_bwd_tc_kernel(const io_t *__restrict__ q, const io_t *__restrict__ k,
                 const float2 qq = make_float2(qv, qv);
                 const float2 kb2 = make_float2(kbr, kbr);
                 float2 aacc = make_float2(0.f, 0.f), kacc = make_float2(0.f, 0.f);
+                // row r's 16-byte chunk c of the diagonal block sits at c*64 + roff floats
+                const int roff = (r >> 3) * 32 + (r & 7) * 4;
                 // pairs (2m, 2m+1) cover s < r; for odd r the last pair is (r-1, r) and
                 // carries the diagonal term (E = 1, dAkk[r][r] outside the support -> 0)
 #pragma unroll
                 for (int c = 0; c < (r + 3) / 4; ++c) {
-                    const float4 aq4 = *reinterpret_cast<const float4 *>(dgq + r * 16 + 4 * c);
-                    const float4 ak4 = *reinterpret_cast<const float4 *>(dgk + r * 16 + 4 * c);
+                    const float4 aq4 = *reinterpret_cast<const float4 *>(dgq + c * 64 + roff);
+                    const float4 ak4 = *reinterpret_cast<const float4 *>(dgk + c * 64 + roff);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int m = 2 * c + h;
@@ -330,7 +357,7 @@ kda_intra_bwd_tc_kernel(const io_t *__restrict__ q, const io_t *__restrict__ k,
                 accq[r] = aacc.x + aacc.y;
                 acck[r] = kacc.x + kacc.y;
                 if ((r & 1) == 0) {  // even r: the diagonal term on its own
-                    const float aqd = dgq[r * 16 + r];
+                    const float aqd = dgq[(r >> 2) * 64 + roff + (r & 3)];
                     accq[r] = fmaf(aqd, kv, accq[r]);
                     dkt2[r >> 1].x = fmaf(aqd, qv, dkt2[r >> 1].x);
                 }
@@ -338,8 +365,7 @@ kda_intra_bwd_tc_kernel(const io_t *__restrict__ q, const io_t *__restrict__ k,
         }
 
         // ---- cross terms: wait for the MMAs, apply the post-factors ----
-        const bool ok = tc::mbar_wait(mbar, phase, MBAR_SPIN_LIMIT);
-        phase ^= 1u;
+        ok &= tc::mbar_wait(mbar, (uint32_t)it & 1u, SPIN_LIMIT);
         tc::fence_after_sync();
         if (i > 0) {
             float f[BC], x[BC];
@@ -376,7 +402,7 @@ kda_intra_bwd_tc_kernel(const io_t *__restrict__ q, const io_t *__restrict__ k,
                 dkt2[m] = __ffma2_rn(make_float2(p[2 * m], p[2 * m + 1]),
                                      make_float2(y[2 * m], y[2 * m + 1]), dkt2[m]);
         }
-        if (!ok) {  // the MMAs never signalled: poison this unit instead of hanging
+        if (!ok) {  // a wait gave up: poison this unit instead of hanging
             const float nan = __int_as_float(0x7fc00000);
 #pragma unroll
             for (int r = 0; r < BC; ++r) accq[r] = acck[r] = nan;
@@ -385,6 +411,7 @@ kda_intra_bwd_tc_kernel(const io_t *__restrict__ q, const io_t *__restrict__ k,
         }
 
         // ---- epilogue ----
+        const Unit un = decode_unit(u, H, NT);
         float dbv[BC];
         {
             const size_t base = grow(un, r0, T, H) * KD + d;
@@ -417,15 +444,25 @@ kda_intra_bwd_tc_kernel(const io_t *__restrict__ q, const io_t *__restrict__ k,
         }
         dbv[0] += __shfl_xor_sync(0xffffffffu, dbv[0], 1);
         if ((lane & 1) == 0) sdbp[(warp & 3) * BT + r0 + (lane >> 1)] = dbv[0];
+        tc::named_bar_sync(1 + i, 128);
+        if ((warp & 3) == 0 && lane < BC) {
+            const int row = r0 + lane;
+            db[grow(un, row, T, H)] = (sdbp[row] + sdbp[BT + row]) +
+                                      (sdbp[2 * BT + row] + sdbp[3 * BT + row]);
+        }
+
+        // ---- unit done: the last warp releases the stage and refills it ----
         tc::fence_before_sync();
-        __syncthreads();
-        if (tid < BT)
-            db[grow(un, tid, T, H)] = (sdbp[tid] + sdbp[BT + tid]) +
-                                      (sdbp[2 * BT + tid] + sdbp[3 * BT + tid]);
-        tc::fence_after_sync();
+        __syncwarp();
+        prev = 0;
+        if (lane == 0) prev = tc::atomic_add_acq_rel_smem(done_count, 1u);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if ((prev % TC_WARPS) == TC_WARPS - 1 && u + 2 * stride < units) {
+            tc::fence_proxy_async_smem();
+            load_unit(st, &full[sidx], tm, beta, u + 2 * stride, T, H, lane);
+        }
     }
 
-    cp_async_wait_group<0>();
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) {
@@ -434,7 +471,70 @@ kda_intra_bwd_tc_kernel(const io_t *__restrict__ q, const io_t *__restrict__ k,
     }
 }
 
+// ---------------------------------------------------------------- host side
+
 int g_num_sms[64];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+cudaError_t get_encoder() {
+    if (g_encode) return cudaSuccess;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return cudaSuccess;
+}
+
+cudaError_t encode(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *base,
+                   const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box,
+                   CUtensorMapL2promotion l2 = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(m, dt, (cuuint32_t)rank, const_cast<void *>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, l2,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_maps(const BwdArgs &a, TmaMaps *tm) {
+    cudaError_t e = get_encoder();
+    if (e != cudaSuccess) return e;
+    const cuuint64_t rows = (cuuint64_t)a.B * a.T, H = (cuuint64_t)a.H;
+    const CUtensorMapDataType io =
+        a.fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    {  // q, k: (channel, head, token row); one unit = box (128, 1, 64)
+        const cuuint64_t dims[3] = {KD, H, rows};
+        const cuuint64_t str[2] = {KD * 2, H * KD * 2};
+        const cuuint32_t box[3] = {KD, 1, BT};
+        if ((e = encode(&tm->q, io, 3, a.q, dims, str, box)) != cudaSuccess) return e;
+        if ((e = encode(&tm->k, io, 3, a.k, dims, str, box)) != cudaSuccess) return e;
+    }
+    {  // g
+        const cuuint64_t dims[3] = {KD, H, rows};
+        const cuuint64_t str[2] = {KD * 4, H * KD * 4};
+        const cuuint32_t box[3] = {KD, 1, BT};
+        if ((e = encode(&tm->g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.g, dims, str, box)) !=
+            cudaSuccess)
+            return e;
+    }
+    {  // dA: (col%4, row%8, row/8, col/4, head); one box = one 16x16 block laid out as a
+       // tensor-core operand (4 floats, 8 rows, 2 row groups, 4 column chunks)
+        const cuuint64_t dims[5] = {4, 8, rows / 8, BT / 4, H};
+        const cuuint64_t str[4] = {H * BT * 4, 8 * H * BT * 4, 16, BT * 4};
+        const cuuint32_t box[5] = {4, 8, 2, 4, 1};
+        // no L2 promotion: a promoted fetch would also pull the rows' unused upper part
+        const CUtensorMapL2promotion l2 = CU_TENSOR_MAP_L2_PROMOTION_NONE;
+        if ((e = encode(&tm->daqk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, a.dAqk, dims, str, box,
+                        l2)) != cudaSuccess)
+            return e;
+        if ((e = encode(&tm->dakk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, a.dAkk, dims, str, box,
+                        l2)) != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
+}
 
 template <typename io_t>
 cudaError_t launch_typed(const BwdArgs &a, cudaStream_t stream) {
@@ -450,11 +550,12 @@ cudaError_t launch_typed(const BwdArgs &a, cudaStream_t stream) {
             return e;
         if (dev >= 0 && dev < 64) g_num_sms[dev] = nsm;
     }
+    TmaMaps tm;
+    if ((e = make_maps(a, &tm)) != cudaSuccess) return e;
     const long long units = (long long)a.B * a.H * (a.T / BT);
     const unsigned grid = (unsigned)(units < nsm ? units : nsm);
-    kern<<<grid, TC_THREADS, SM_TOTAL, stream>>>((const io_t *)a.q, (const io_t *)a.k, a.g,
-                                                 a.beta, a.dAqk, a.dAkk, a.dq, a.dk, a.db,
-                                                 a.dg, a.T, a.H, units);
+    kern<<<grid, TC_THREADS, SM_TOTAL, stream>>>(tm, a.beta, a.dq, a.dk, a.db, a.dg, a.T, a.H,
+                                                 units);
     return cudaGetLastError();
 }
 

@@ -78,6 +78,7 @@ def fake_args(B=1, T=64, H=1, dtype=0, **override):
     (dict(B=0), ERR_SHAPE),
     (dict(H=-1), ERR_SHAPE),
     (dict(H=65537), ERR_SHAPE),
+    (dict(B=1 << 16, T=1 << 16), ERR_SHAPE),
     (dict(B=1 << 20, T=1 << 20, H=64), ERR_SHAPE),
     (dict(dtype=2), ERR_DTYPE),
     (dict(dtype=-1), ERR_DTYPE),
