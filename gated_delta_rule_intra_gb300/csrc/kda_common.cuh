@@ -49,11 +49,13 @@ __device__ __forceinline__ void cp_async_wait_all() {
 struct Unit {
     int b, h, c;
 };
+// (The host rejects problems with 2^31 or more units, so 32-bit division suffices.)
 __device__ __forceinline__ Unit decode_unit(long long u, int H, int NT) {
+    const unsigned uu = (unsigned)u, q = uu / (unsigned)H;
     Unit x;
-    x.h = (int)(u % H);
-    x.c = (int)((u / H) % NT);
-    x.b = (int)(u / ((long long)H * NT));
+    x.h = (int)(uu - q * (unsigned)H);
+    x.c = (int)(q % (unsigned)NT);
+    x.b = (int)(q / (unsigned)NT);
     return x;
 }
 
