@@ -57,14 +57,20 @@ def algorithmic_bytes_per_unit(qk_bytes: int = 2) -> int:
     return qk + g + beta + da + out
 
 
-def source_hash() -> str:
+KERNEL_SOURCES = {
+    "kda_intra_bwd_tc_kernel": ("kda_intra_tc.cu", "tc_ptx.cuh", "kda_common.cuh"),
+    "kda_intra_bwd_fp32_kernel": ("kda_intra_fp32.cu", "kda_common.cuh"),
+}
+
+
+def source_hash(kernel: str) -> str:
+    """Hash of the source files one kernel is compiled from (ties an ncu summary to
+    the code it measured)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_intra_gb300", "csrc")
-    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc))
-    files.append(os.path.join(ROOT, "include", "kda.h"))
-    for f in files:
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode())
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -89,7 +95,7 @@ def ncu_traffic(kernel: str, workload: str):
                 if ":" in line:
                     k, v = line.split(":", 1)
                     fields[k.strip()] = v.strip()
-        if fields.get("source_sha256") != source_hash():
+        if fields.get("source_sha256") != source_hash(kernel):
             return None
         return float(fields["dram_bytes_per_launch"])
     except Exception:
