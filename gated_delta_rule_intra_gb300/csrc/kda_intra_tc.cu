@@ -310,58 +310,99 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         }
         __syncwarp();
 
-        // ---- diagonal block: one exp2 per (r, s, d), shared by both sides, computed
-        // two source rows at a time with packed FP32x2 arithmetic ----
-        float accq[BC], acck[BC];
+        // ---- diagonal block: one exp2 per (r, s, d), shared by both sides, two source
+        // rows at a time in packed FP32x2.  Rows run in descending order: once row r is
+        // processed, its row sums and its column sum dkt[r] are complete, so each row is
+        // written out right away.  Rows 15..8 (92 of the 120 pairs) run before the MMA
+        // result is needed; rows 7..0 after it. ----
+        float accq[BC], acck[BC], dbv[BC];
         float2 dkt2[BC / 2];
 #pragma unroll
         for (int m = 0; m < BC / 2; ++m) dkt2[m] = make_float2(0.f, 0.f);
-        {
-            const float *dgq = reinterpret_cast<const float *>(st + ST_DQ) + dablk(i, i) * 256;
-            const float *dgk = reinterpret_cast<const float *>(st + ST_DK) + dablk(i, i) * 256;
-            const float2 neg1 = make_float2(-1.f, -1.f);
+        const float *dgq = reinterpret_cast<const float *>(st + ST_DQ) + dablk(i, i) * 256;
+        const float *dgk = reinterpret_cast<const float *>(st + ST_DK) + dablk(i, i) * 256;
+        const float2 neg1 = make_float2(-1.f, -1.f);
+        const Unit un = decode_unit(u, H, NT);
+        const size_t obase = grow(un, r0, T, H) * KD + d;
+        const uint32_t hk = (uint32_t)H * KD;
+
+        auto diag_row = [&](const int r) {
+            const float gv = KDA_EL(g2, r), kv = KDA_EL(k2, r);
+            const float qv = to_f32(sq[(r0 + r) * KD + d]);
+            const float kbr = sbeta[r0 + r] * kv;
+            const float2 grr = make_float2(gv, gv);
+            const float2 qq = make_float2(qv, qv);
+            const float2 kb2 = make_float2(kbr, kbr);
+            float2 aacc = make_float2(0.f, 0.f), kacc = make_float2(0.f, 0.f);
+            // row r's 16-byte chunk c of the diagonal block sits at c*64 + roff floats
+            const int roff = (r >> 3) * 32 + (r & 7) * 4;
+            // pairs (2m, 2m+1) cover s < r; for odd r the last pair is (r-1, r) and
+            // carries the diagonal term (E = 1, dAkk[r][r] outside the support -> 0)
 #pragma unroll
-            for (int r = 0; r < BC; ++r) {
-                const float gv = KDA_EL(g2, r), kv = KDA_EL(k2, r);
-                const float qv = to_f32(sq[(r0 + r) * KD + d]);
-                const float kbr = sbeta[r0 + r] * kv;
-                const float2 grr = make_float2(gv, gv);
-                const float2 qq = make_float2(qv, qv);
-                const float2 kb2 = make_float2(kbr, kbr);
-                float2 aacc = make_float2(0.f, 0.f), kacc = make_float2(0.f, 0.f);
-                // row r's 16-byte chunk c of the diagonal block sits at c*64 + roff floats
-                const int roff = (r >> 3) * 32 + (r & 7) * 4;
-                // pairs (2m, 2m+1) cover s < r; for odd r the last pair is (r-1, r) and
-                // carries the diagonal term (E = 1, dAkk[r][r] outside the support -> 0)
+            for (int c = 0; c < (r + 3) / 4; ++c) {
+                const float4 aq4 = *reinterpret_cast<const float4 *>(dgq + c * 64 + roff);
+                const float4 ak4 = *reinterpret_cast<const float4 *>(dgk + c * 64 + roff);
 #pragma unroll
-                for (int c = 0; c < (r + 3) / 4; ++c) {
-                    const float4 aq4 = *reinterpret_cast<const float4 *>(dgq + c * 64 + roff);
-                    const float4 ak4 = *reinterpret_cast<const float4 *>(dgk + c * 64 + roff);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int m = 2 * c + h;
-                        if (2 * m < r) {
-                            const float2 aq = h ? make_float2(aq4.z, aq4.w) : make_float2(aq4.x, aq4.y);
-                            float2 ak = h ? make_float2(ak4.z, ak4.w) : make_float2(ak4.x, ak4.y);
-                            if (2 * m + 1 == r) ak.y = 0.f;
-                            const float2 df = __ffma2_rn(g2[m], neg1, grr);
-                            const float2 ev = make_float2(ex2(df.x), ex2(df.y));
-                            const float2 tq = __fmul2_rn(k2[m], ev);
-                            aacc = __ffma2_rn(aq, tq, aacc);
-                            kacc = __ffma2_rn(ak, tq, kacc);
-                            const float2 uu = __ffma2_rn(aq, qq, __fmul2_rn(ak, kb2));
-                            dkt2[m] = __ffma2_rn(uu, ev, dkt2[m]);
-                        }
+                for (int h = 0; h < 2; ++h) {
+                    const int m = 2 * c + h;
+                    if (2 * m < r) {
+                        const float2 aq = h ? make_float2(aq4.z, aq4.w) : make_float2(aq4.x, aq4.y);
+                        float2 ak = h ? make_float2(ak4.z, ak4.w) : make_float2(ak4.x, ak4.y);
+                        if (2 * m + 1 == r) ak.y = 0.f;
+                        const float2 df = __ffma2_rn(g2[m], neg1, grr);
+                        const float2 ev = make_float2(ex2(df.x), ex2(df.y));
+                        const float2 tq = __fmul2_rn(k2[m], ev);
+                        aacc = __ffma2_rn(aq, tq, aacc);
+                        kacc = __ffma2_rn(ak, tq, kacc);
+                        const float2 uu = __ffma2_rn(aq, qq, __fmul2_rn(ak, kb2));
+                        dkt2[m] = __ffma2_rn(uu, ev, dkt2[m]);
                     }
                 }
-                accq[r] = aacc.x + aacc.y;
-                acck[r] = kacc.x + kacc.y;
-                if ((r & 1) == 0) {  // even r: the diagonal term on its own
-                    const float aqd = dgq[(r >> 2) * 64 + roff + (r & 3)];
-                    accq[r] = fmaf(aqd, kv, accq[r]);
-                    dkt2[r >> 1].x = fmaf(aqd, qv, dkt2[r >> 1].x);
+            }
+            accq[r] += aacc.x + aacc.y;
+            acck[r] += kacc.x + kacc.y;
+            if ((r & 1) == 0) {  // even r: the diagonal term on its own
+                const float aqd = dgq[(r >> 2) * 64 + roff + (r & 3)];
+                accq[r] = fmaf(aqd, kv, accq[r]);
+                dkt2[r >> 1].x = fmaf(aqd, qv, dkt2[r >> 1].x);
+            }
+        };
+        auto out_row = [&](const int r) {
+            const int row = r0 + r;
+            const size_t off = obase + (size_t)((uint32_t)r * hk);
+            const float qv = to_f32(sq[row * KD + d]);
+            const float kv = KDA_EL(k2, r), dkv = KDA_EL(dkt2, r);
+            const float pk = sbeta[row] * acck[r];
+            dq[off] = accq[r];
+            dk[off] = pk + dkv;
+            dg[off] = LN2 * fmaf(qv, accq[r], (pk - dkv) * kv);
+            dbv[r] = acck[r] * kv;
+        };
+        // db[r] = sum over d of 8 rows at a time: transpose-reduce across the warp's lanes
+        // (lane l ends with row (l>>2)&7), then a fixed-order sum over the block's 4 warps.
+        auto db_rows = [&](const int rbase) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = dbv[rbase + j];
+#pragma unroll
+            for (int w = 4, m = 16; w >= 1; w >>= 1, m >>= 1) {
+                const bool hi = (lane & m) != 0;
+#pragma unroll
+                for (int j = 0; j < w; ++j) {
+                    const float send = hi ? v[j] : v[j + w];
+                    const float keep = hi ? v[j + w] : v[j];
+                    v[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
                 }
             }
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+            if ((lane & 3) == 0) sdbp[(warp & 3) * BT + r0 + rbase + (lane >> 2)] = v[0];
+        };
+
+#pragma unroll
+        for (int r = BC - 1; r >= BC / 2; --r) {
+            accq[r] = acck[r] = 0.f;
+            diag_row(r);
         }
 
         // ---- cross terms: wait for the MMAs, apply the post-factors ----
@@ -373,11 +414,14 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             tc::tmem_ld16(tlane + TM_XQ + 16 * (i - 1), x);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int r = 0; r < BC; ++r) accq[r] = fmaf(f[r], x[r], accq[r]);
+            for (int r = 0; r < BC; ++r) accq[r] = fmaf(f[r], x[r], r >= BC / 2 ? accq[r] : 0.f);
             tc::tmem_ld16(tlane + TM_XK + 16 * (i - 1), x);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int r = 0; r < BC; ++r) acck[r] = fmaf(f[r], x[r], acck[r]);
+            for (int r = 0; r < BC; ++r) acck[r] = fmaf(f[r], x[r], r >= BC / 2 ? acck[r] : 0.f);
+        } else {
+#pragma unroll
+            for (int r = 0; r < BC / 2; ++r) accq[r] = acck[r] = 0.f;
         }
         if (i < NBLK - 1) {
             float y[BC], p[BC];
@@ -410,40 +454,17 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             for (int m = 0; m < BC / 2; ++m) dkt2[m] = make_float2(nan, nan);
         }
 
-        // ---- epilogue ----
-        const Unit un = decode_unit(u, H, NT);
-        float dbv[BC];
-        {
-            const size_t base = grow(un, r0, T, H) * KD + d;
-            const uint32_t hk = (uint32_t)H * KD;
+        // ---- rows 15..8 are complete: write them; then rows 7..0 ----
 #pragma unroll
-            for (int r = 0; r < BC; ++r) {
-                const int row = r0 + r;
-                const size_t off = base + (size_t)((uint32_t)r * hk);
-                const float qv = to_f32(sq[row * KD + d]);
-                const float kv = KDA_EL(k2, r), dkv = KDA_EL(dkt2, r);
-                const float pk = sbeta[row] * acck[r];
-                dq[off] = accq[r];
-                dk[off] = pk + dkv;
-                dg[off] = LN2 * fmaf(qv, accq[r], (pk - dkv) * kv);
-                dbv[r] = acck[r] * kv;
-            }
+        for (int r = BC - 1; r >= BC / 2; --r) out_row(r);
+        db_rows(BC / 2);
+#pragma unroll
+        for (int r = BC / 2 - 1; r >= 0; --r) {
+            diag_row(r);
+            out_row(r);
         }
+        db_rows(0);
 #undef KDA_EL
-        // db[r] = sum over d: transpose-reduce the 16 row sums across the warp's lanes,
-        // lane l ends with row l>>1; then a fixed-order sum over the block's 4 warps.
-#pragma unroll
-        for (int w = 8, m = 16; w >= 1; w >>= 1, m >>= 1) {
-            const bool hi = (lane & m) != 0;
-#pragma unroll
-            for (int j = 0; j < w; ++j) {
-                const float send = hi ? dbv[j] : dbv[j + w];
-                const float keep = hi ? dbv[j + w] : dbv[j];
-                dbv[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-            }
-        }
-        dbv[0] += __shfl_xor_sync(0xffffffffu, dbv[0], 1);
-        if ((lane & 1) == 0) sdbp[(warp & 3) * BT + r0 + (lane >> 1)] = dbv[0];
         tc::named_bar_sync(1 + i, 128);
         if ((warp & 3) == 0 && lane < BC) {
             const int row = r0 + lane;
