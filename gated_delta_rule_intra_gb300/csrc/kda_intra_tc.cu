@@ -193,6 +193,29 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         const io_t *sk = reinterpret_cast<const io_t *>(st + ST_K);
         const float *sbeta = reinterpret_cast<const float *>(st + ST_BETA);
 
+        // ---- column-side B operands: dA blocks (j, 0..j-1) transposed.  The loads go
+        // out first so their latency overlaps the column loads and the prescale. ----
+        float trq[3], trk[3];
+        int trdst[3];
+        {
+            const float *aq = reinterpret_cast<const float *>(st + ST_DQ);
+            const float *ak = reinterpret_cast<const float *>(st + ST_DK);
+#pragma unroll
+            for (int x = 0; x < 3; ++x) {
+                const int idx = tid + x * TC_THREADS;  // < 1536
+                const int j = idx >= 768 ? 3 : idx >= 256 ? 2 : 1;
+                const int e = idx - 128 * j * (j - 1);
+                // e enumerates the destination floats in order (n/8, k/4, n%8, k%4)
+                const int n = (e >> 7) * 8 + ((e >> 2) & 7);  // s
+                const int kk = ((e >> 5) & 3) * 4 + (e & 3);  // r - 16j
+                const int src = dablk(j, n >> 4) * 256 + ((n & 15) >> 2) * 64 + (kk >> 3) * 32 +
+                                (kk & 7) * 4 + (n & 3);
+                trdst[x] = (int)bcol_off(j) / 4 + e;
+                trq[x] = aq[src];
+                trk[x] = ak[src];
+            }
+        }
+
         // this thread's column of its block, as (even row, odd row) pairs
         float2 g2[BC / 2], k2[BC / 2];
 #pragma unroll
@@ -242,25 +265,13 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             tc::tmem_st16(tlane + TM_AKBB + 16 * (i - 1), v);
         }
 
-        // ---- column-side B operands: dA blocks (j, 0..j-1) transposed ----
         {
-            const float *aq = reinterpret_cast<const float *>(st + ST_DQ);
-            const float *ak = reinterpret_cast<const float *>(st + ST_DK);
             float *cq = reinterpret_cast<float *>(smem + SM_BCQ);
             float *ck = reinterpret_cast<float *>(smem + SM_BCK);
 #pragma unroll
             for (int x = 0; x < 3; ++x) {
-                const int idx = tid + x * TC_THREADS;  // < 1536
-                const int j = idx >= 768 ? 3 : idx >= 256 ? 2 : 1;
-                const int e = idx - 128 * j * (j - 1);
-                // e enumerates the destination floats in order (n/8, k/4, n%8, k%4)
-                const int n = (e >> 7) * 8 + ((e >> 2) & 7);  // s
-                const int kk = ((e >> 5) & 3) * 4 + (e & 3);  // r - 16j
-                const int src = dablk(j, n >> 4) * 256 + ((n & 15) >> 2) * 64 + (kk >> 3) * 32 +
-                                (kk & 7) * 4 + (n & 3);
-                const int dst = (int)bcol_off(j) / 4 + e;
-                cq[dst] = aq[src];
-                ck[dst] = ak[src];
+                cq[trdst[x]] = trq[x];
+                ck[trdst[x]] = trk[x];
             }
         }
 
