@@ -45,16 +45,20 @@ KERNEL_NAMES = {
 }
 
 
-def algorithmic_bytes_per_unit(qk_bytes: int = 2) -> int:
-    """Bytes one unit must move at minimum: q, k, g, beta, the ten lower 16x16
-    blocks of dAqk and dAkk, and the dq, dk, dg, db outputs."""
+def algorithmic_bytes_per_unit(qk_bytes: int = 2, group: int = 1, accumulate: bool = False,
+                               io_out: bool = False) -> float:
+    """Bytes one unit must move at minimum: q, k (shared by `group` value heads),
+    g, beta, the ten lower 16x16 blocks of dAqk and dAkk, the dq, dk, dg, db outputs
+    (dq, dk in the io dtype when `io_out`), and the incoming gradients when
+    `accumulate`."""
     bt, kd, bc = kda_inputs.BT, kda_inputs.K, 16
-    qk = 2 * bt * kd * qk_bytes
+    qk = 2 * bt * kd * qk_bytes / group
     g = bt * kd * 4
     beta = bt * 4
     da = 2 * 10 * bc * bc * 4
-    out = 3 * bt * kd * 4 + bt * 4
-    return qk + g + beta + da + out
+    out = 2 * bt * kd * (qk_bytes if io_out else 4) + bt * kd * 4 + bt * 4
+    acc = 3 * bt * kd * 4 + bt * 4 if accumulate else 0
+    return qk + g + beta + da + out + acc
 
 
 KERNEL_SOURCES = {
@@ -198,8 +202,8 @@ def max_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
-def config_dict(cfg, path):
-    return {
+def config_dict(cfg, path, opts=None):
+    d = {
         "workload": cfg.name, "B": cfg.B, "T": cfg.T, "H": cfg.H, "K": kda_inputs.K,
         "BT": kda_inputs.BT, "BC": 16, "units": cfg.units,
         "qk_dtype": str(cfg.qk_dtype).replace("torch.", ""),
@@ -207,6 +211,9 @@ def config_dict(cfg, path):
         "l2": "no flush: inputs+outputs of one step (%.2f GB) exceed the 129 MB L2"
               % (cfg.units * algorithmic_bytes_per_unit() / 1e9),
     }
+    if opts:
+        d["options"] = opts
+    return d
 
 
 # --------------------------------------------------------------------------- oracle
@@ -306,13 +313,35 @@ def run_ours(args, cfg):
     seed = kda_inputs.SEED0 + args.config + 1000 * rank
     cpu = kda_inputs.make_inputs(cfg.B, cfg.T, cfg.H, gate_lo=cfg.gate_lo,
                                  qk_dtype=cfg.qk_dtype, seed=seed)
+    if args.gva > 1:  # q/k shared by groups of value heads
+        cpu["q"] = cpu["q"][:, :, ::args.gva].contiguous()
+        cpu["k"] = cpu["k"][:, :, ::args.gva].contiguous()
     x = {n: v.to(dev) for n, v in cpu.items()}
-    fn = getattr(kda, args.path)
     ins = [x[n] for n in ("q", "k", "g", "beta", "dAqk", "dAkk")]
-    outs = kda._outputs(x["q"], None, None, None, None)
+    extended = args.gva > 1 or args.accumulate or args.fold_dg or args.io_dtype_out
+    opts = None
+    if extended:
+        gen = torch.Generator().manual_seed(seed + 1)
+        extra = {}
+        if args.accumulate:
+            shp = (cfg.B, cfg.T, cfg.H, kda_inputs.K)
+            extra = {n: torch.randn(*shp, generator=gen).to(dev)
+                     for n in ("dq_in", "dk_in", "dg_in")}
+            extra["db_in"] = torch.randn(cfg.B, cfg.T, cfg.H, generator=gen).to(dev)
+        outs = list(kda.kda_intra_bwd_ex(*ins, **extra, fold_dg=args.fold_dg,
+                                         dqdk_io_dtype=args.io_dtype_out))
+        opts = {"value_heads_per_qk_head": args.gva, "accumulate": args.accumulate,
+                "fold_dg": args.fold_dg, "dqdk_io_dtype": args.io_dtype_out}
 
-    def step():
-        fn(*ins, *outs, stream=stream)
+        def step():
+            kda.kda_intra_bwd_ex(*ins, *outs, **extra, fold_dg=args.fold_dg,
+                                 dqdk_io_dtype=args.io_dtype_out, stream=stream)
+    else:
+        fn = getattr(kda, args.path)
+        outs = kda._outputs(x["q"], None, None, None, None)
+
+        def step():
+            fn(*ins, *outs, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -340,7 +369,7 @@ def run_ours(args, cfg):
 
     # end to end through the host-buffer entry point
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not extended:
         pin = {n: v.pin_memory() for n, v in cpu.items()}
         hout = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
         ws = torch.empty(kda.kda_intra_bwd_host_workspace_bytes(cfg.B, cfg.T, cfg.H,
@@ -369,14 +398,15 @@ def run_ours(args, cfg):
         del ws
 
     cpu_base = None
-    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+    if world == 1 and rank == 0 and not args.no_cpu_baseline and not extended:
         cpu_base = cpu_baseline(cpu, cfg)
         cpu_base["parity_check"] = sampled_check(cpu, cfg, outs)
 
     if rank != 0:
         return
     bytes_per_launch = cfg.units * algorithmic_bytes_per_unit(
-        torch.tensor([], dtype=cfg.qk_dtype).element_size())
+        torch.tensor([], dtype=cfg.qk_dtype).element_size(), group=args.gva,
+        accumulate=args.accumulate, io_out=args.io_dtype_out)
     achieved = bytes_per_launch / (ms / args.steps / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
     kname = KERNEL_NAMES[args.path]
@@ -388,7 +418,8 @@ def run_ours(args, cfg):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32" if args.path.endswith("fp32") else "tf32+f32",
-        "data": "synthetic", "config": config_dict(cfg, args.path),
+        "data": "synthetic",
+        "config": config_dict(cfg, "kda_intra_bwd_ex" if extended else args.path, opts),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
@@ -414,6 +445,14 @@ def main():
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--gva", type=int, default=1,
+                   help="value heads per q/k head (kda_intra_bwd_ex); heads stay H")
+    p.add_argument("--accumulate", action="store_true",
+                   help="add incoming dq/dk/dg/db in-kernel (kda_intra_bwd_ex)")
+    p.add_argument("--fold-dg", action="store_true",
+                   help="dg as its chunk-local reverse cumsum (kda_intra_bwd_ex)")
+    p.add_argument("--io-dtype-out", action="store_true",
+                   help="dq, dk written in the q/k dtype (kda_intra_bwd_ex)")
     args = p.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     cfg = kda_inputs.CONFIGS[args.config]

@@ -8,6 +8,9 @@ The functions carry the C names of ``include/kda.h``:
 
 * ``kda_intra_bwd``       -- fast path (TF32 tensor-core cross terms)
 * ``kda_intra_bwd_fp32``  -- all-FP32 path
+* ``kda_intra_bwd_ex``    -- fast path with options: grouped value heads, incoming
+  gradients added in-kernel, dg folded to its chunk-local reverse cumsum, dq/dk in
+  the q/k dtype
 * ``kda_intra_bwd_host``  -- host buffers in and out, copies on the stream
 * ``kda_status_str``, ``kda_abi_version``
 """
@@ -30,6 +33,13 @@ K = 128
 
 _DTYPES = {torch.bfloat16: KDA_BF16, torch.float16: KDA_FP16}
 _lib = None
+
+
+class KdaOpts(ctypes.Structure):
+    """Mirror of kda_intra_bwd_opts_t."""
+    _fields_ = [("HV", ctypes.c_int), ("dq_in", ctypes.c_void_p), ("dk_in", ctypes.c_void_p),
+                ("dg_in", ctypes.c_void_p), ("db_in", ctypes.c_void_p),
+                ("fold_dg", ctypes.c_int), ("dqdk_io_dtype", ctypes.c_int)]
 
 
 class KdaError(RuntimeError):
@@ -55,6 +65,8 @@ def load_library(path: str | None = None):
         f = getattr(lib, name)
         f.argtypes = sig
         f.restype = st
+    lib.kda_intra_bwd_ex.argtypes = sig[:-1] + [ctypes.POINTER(KdaOpts), vp]
+    lib.kda_intra_bwd_ex.restype = st
     lib.kda_intra_bwd_host.argtypes = sig[:-1] + [vp, ctypes.c_size_t, vp]
     lib.kda_intra_bwd_host.restype = st
     lib.kda_intra_bwd_host_workspace_bytes.argtypes = [i, i, i, i]
@@ -160,6 +172,64 @@ def kda_intra_bwd_fp32(q, k, g, beta, dAqk, dAkk, dq=None, dk=None, db=None, dg=
     """Same contract as ``kda_intra_bwd``; every product and sum in FP32."""
     return _device_call("kda_intra_bwd_fp32", q, k, g, beta, dAqk, dAkk, dq, dk, db, dg,
                         stream)
+
+
+def kda_intra_bwd_ex(q, k, g, beta, dAqk, dAkk, dq=None, dk=None, db=None, dg=None, *,
+                     dq_in=None, dk_in=None, dg_in=None, db_in=None, fold_dg=False,
+                     dqdk_io_dtype=False, stream=None):
+    """Intra-chunk backward with the extended options of ``kda_intra_bwd_ex``.
+
+    q, k have H heads; g, beta, dAqk, dAkk, the outputs and the optional incoming
+    gradients have HV = g.shape[2] heads (value head hv reads q/k head hv // (HV // H)).
+    ``dq_in``.. ``db_in`` are added in-kernel (they may be the output tensors
+    themselves); ``fold_dg`` returns dg as its inclusive reverse cumsum inside each
+    64-token chunk; ``dqdk_io_dtype`` writes dq and dk in q's dtype.
+    Returns (dq, dk, db, dg).
+    """
+    if q.device.type != "cuda":
+        raise ValueError("kda_intra_bwd_ex needs CUDA tensors (no CPU path exists)")
+    B, T, H = _shape(q)
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"q/k dtype must be bf16 or fp16, got {q.dtype}")
+    if g.dim() != 4:
+        raise ValueError("g must be [B, T, HV, 128]")
+    HV = g.shape[2]
+    dev, f32 = q.device, torch.float32
+    odt = q.dtype if dqdk_io_dtype else f32
+    dq = torch.empty(B, T, HV, K, device=dev, dtype=odt) if dq is None else dq
+    dk = torch.empty(B, T, HV, K, device=dev, dtype=odt) if dk is None else dk
+    dg = torch.empty(B, T, HV, K, device=dev, dtype=f32) if dg is None else dg
+    db = torch.empty(B, T, HV, device=dev, dtype=f32) if db is None else db
+    _check("q", q, (B, T, H, K), q.dtype, dev)
+    _check("k", k, (B, T, H, K), q.dtype, dev)
+    _check("g", g, (B, T, HV, K), f32, dev)
+    _check("beta", beta, (B, T, HV), f32, dev)
+    _check("dAqk", dAqk, (B, T, HV, BT), f32, dev)
+    _check("dAkk", dAkk, (B, T, HV, BT), f32, dev)
+    _check("dq", dq, (B, T, HV, K), odt, dev)
+    _check("dk", dk, (B, T, HV, K), odt, dev)
+    _check("dg", dg, (B, T, HV, K), f32, dev)
+    _check("db", db, (B, T, HV), f32, dev)
+    opts = KdaOpts()
+    opts.HV = HV
+    for name, t, shape in (("dq_in", dq_in, (B, T, HV, K)), ("dk_in", dk_in, (B, T, HV, K)),
+                           ("dg_in", dg_in, (B, T, HV, K)), ("db_in", db_in, (B, T, HV))):
+        if t is not None:
+            _check(name, t, shape, f32, dev)
+            setattr(opts, name, t.data_ptr())
+    opts.fold_dg = int(bool(fold_dg))
+    opts.dqdk_io_dtype = int(bool(dqdk_io_dtype))
+    lib = load_library()
+    ptr = ctypes.c_void_p
+    with torch.cuda.device(dev):
+        rc = lib.kda_intra_bwd_ex(
+            ptr(q.data_ptr()), ptr(k.data_ptr()), ptr(g.data_ptr()), ptr(beta.data_ptr()),
+            ptr(dAqk.data_ptr()), ptr(dAkk.data_ptr()), ptr(dq.data_ptr()),
+            ptr(dk.data_ptr()), ptr(db.data_ptr()), ptr(dg.data_ptr()),
+            B, T, H, _DTYPES[q.dtype], ctypes.byref(opts), _stream_handle(stream, dev))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_intra_bwd_ex")
+    return dq, dk, db, dg
 
 
 def kda_intra_bwd_host_workspace_bytes(B: int, T: int, H: int, qk_dtype=torch.bfloat16):

@@ -84,6 +84,64 @@ kda_status_t check_device() {
     return ok ? KDA_OK : KDA_ERR_UNSUPPORTED_DEVICE;
 }
 
+// Validation of the extended entry point: q/k have H heads, everything else HV.
+kda_status_t check_ex(const void *q, const void *k, const float *g, const float *beta,
+                      const float *dAqk, const float *dAkk, void *dq, void *dk, float *db,
+                      float *dg, int B, int T, int H, kda_dtype_t dt,
+                      const kda_intra_bwd_opts_t &o) {
+    if (!q || !k || !g || !beta || !dAqk || !dAkk || !dq || !dk || !db || !dg)
+        return KDA_ERR_NULL;
+    const int HV = o.HV ? o.HV : H;
+    if (H <= 0 || HV <= 0 || HV % H != 0) return KDA_ERR_SHAPE;
+    kda_status_t st = check_shape(B, T, HV);
+    if (st != KDA_OK) return st;
+    if (dt != KDA_BF16 && dt != KDA_FP16) return KDA_ERR_DTYPE;
+    if (o.fold_dg != 0 && o.fold_dg != 1) return KDA_ERR_OPTION;
+    if (o.dqdk_io_dtype != 0 && o.dqdk_io_dtype != 1) return KDA_ERR_OPTION;
+    if (o.dqdk_io_dtype && HV != H) return KDA_ERR_OPTION;
+    const void *a16[] = {q, k, g, dAqk, dAkk, dq, dk, dg};
+    for (const void *p : a16)
+        if ((uintptr_t)p % 16u) return KDA_ERR_ALIGN;
+    const void *a4[] = {beta, db, o.dq_in, o.dk_in, o.dg_in, o.db_in};
+    for (const void *p : a4)
+        if ((uintptr_t)p % 4u) return KDA_ERR_ALIGN;
+    const size_t rq = (size_t)B * T * H, rv = (size_t)B * T * HV;
+    const size_t odq = o.dqdk_io_dtype ? 2 : 4;
+    const Range in[] = {
+        {(uintptr_t)q, (uintptr_t)q + rq * KDA_K * 2},
+        {(uintptr_t)k, (uintptr_t)k + rq * KDA_K * 2},
+        {(uintptr_t)g, (uintptr_t)g + rv * KDA_K * 4},
+        {(uintptr_t)beta, (uintptr_t)beta + rv * 4},
+        {(uintptr_t)dAqk, (uintptr_t)dAqk + rv * KDA_BT * 4},
+        {(uintptr_t)dAkk, (uintptr_t)dAkk + rv * KDA_BT * 4},
+    };
+    const Range opt_in[] = {
+        {(uintptr_t)o.dq_in, o.dq_in ? (uintptr_t)o.dq_in + rv * KDA_K * 4 : 0},
+        {(uintptr_t)o.dk_in, o.dk_in ? (uintptr_t)o.dk_in + rv * KDA_K * 4 : 0},
+        {(uintptr_t)o.db_in, o.db_in ? (uintptr_t)o.db_in + rv * 4 : 0},
+        {(uintptr_t)o.dg_in, o.dg_in ? (uintptr_t)o.dg_in + rv * KDA_K * 4 : 0},
+    };
+    const Range out[] = {
+        {(uintptr_t)dq, (uintptr_t)dq + rv * KDA_K * odq},
+        {(uintptr_t)dk, (uintptr_t)dk + rv * KDA_K * odq},
+        {(uintptr_t)db, (uintptr_t)db + rv * 4},
+        {(uintptr_t)dg, (uintptr_t)dg + rv * KDA_K * 4},
+    };
+    for (int a = 0; a < 4; ++a) {
+        for (const Range &r : in)
+            if (overlaps(out[a], r)) return KDA_ERR_OVERLAP;
+        for (int b = a + 1; b < 4; ++b)
+            if (overlaps(out[a], out[b])) return KDA_ERR_OVERLAP;
+        for (int b = 0; b < 4; ++b) {
+            if (!opt_in[b].lo) continue;
+            // an incoming gradient may be its own output exactly (in place), nothing else
+            const bool same = (a == b) && opt_in[b].lo == out[a].lo && opt_in[b].hi == out[a].hi;
+            if (!same && overlaps(out[a], opt_in[b])) return KDA_ERR_OVERLAP;
+        }
+    }
+    return KDA_OK;
+}
+
 kda::BwdArgs pack(const void *q, const void *k, const float *g, const float *beta,
                   const float *dAqk, const float *dAkk, float *dq, float *dk, float *db,
                   float *dg, int B, int T, int H, kda_dtype_t dt) {
@@ -113,6 +171,31 @@ kda_status_t kda_intra_bwd_fp32(const void *q, const void *k, const float *g,
     const kda::BwdArgs a = pack(q, k, g, beta, dAqk, dAkk, dq, dk, db, dg, B, T, H, qk_dtype);
     return kda::launch_intra_fp32(a, (cudaStream_t)stream) == cudaSuccess ? KDA_OK
                                                                           : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_intra_bwd_ex(const void *q, const void *k, const float *g,
+                              const float *beta, const float *dAqk, const float *dAkk,
+                              void *dq, void *dk, float *db, float *dg, int B, int T, int H,
+                              kda_dtype_t qk_dtype, const kda_intra_bwd_opts_t *opts,
+                              kda_stream_t stream) {
+    kda_intra_bwd_opts_t o;
+    memset(&o, 0, sizeof(o));
+    if (opts) o = *opts;
+    kda_status_t st = check_ex(q, k, g, beta, dAqk, dAkk, dq, dk, db, dg, B, T, H, qk_dtype, o);
+    if (st != KDA_OK) return st;
+    if ((st = check_device()) != KDA_OK) return st;
+    (void)cudaGetLastError();
+    kda::BwdArgs a = pack(q, k, g, beta, dAqk, dAkk, (float *)dq, (float *)dk, db, dg, B, T,
+                          H, qk_dtype);
+    a.HV = o.HV ? o.HV : H;
+    a.dq_in = o.dq_in;
+    a.dk_in = o.dk_in;
+    a.dg_in = o.dg_in;
+    a.db_in = o.db_in;
+    a.fold_dg = o.fold_dg != 0;
+    a.emit_io = o.dqdk_io_dtype != 0;
+    return kda::launch_intra_tc(a, (cudaStream_t)stream) == cudaSuccess ? KDA_OK
+                                                                        : KDA_ERR_CUDA;
 }
 
 kda_status_t kda_intra_bwd(const void *q, const void *k, const float *g, const float *beta,
@@ -202,6 +285,7 @@ const char *kda_status_str(kda_status_t status) {
             return "KDA_ERR_UNSUPPORTED_DEVICE: needs compute capability 10.3 (sm_103a)";
         case KDA_ERR_OVERLAP: return "KDA_ERR_OVERLAP: argument buffers overlap";
         case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing or too small";
+        case KDA_ERR_OPTION: return "KDA_ERR_OPTION: unsupported option combination";
     }
     return "KDA_ERR_UNKNOWN";
 }

@@ -198,8 +198,8 @@ cudaError_t launch_typed(const BwdArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const long long units = (long long)a.B * a.H * (a.T / BT);
     kern<<<(unsigned)units, FP32_THREADS, smem, stream>>>(
-        (const io_t *)a.q, (const io_t *)a.k, a.g, a.beta, a.dAqk, a.dAkk, a.dq, a.dk,
-        a.db, a.dg, a.T, a.H);
+        (const io_t *)a.q, (const io_t *)a.k, a.g, a.beta, a.dAqk, a.dAkk, (float *)a.dq,
+        (float *)a.dk, a.db, a.dg, a.T, a.H);
     return cudaGetLastError();
 }
 

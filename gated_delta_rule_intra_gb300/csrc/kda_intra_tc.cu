@@ -67,6 +67,11 @@ constexpr int SM_MMA = SM_FULL + 16;         // MMAs-done mbarrier
 constexpr int SM_CNT = SM_MMA + 8;           // operand counter, unit-done counter
 constexpr int SM_TSLOT = SM_CNT + 8;
 constexpr int SM_TOTAL = SM_TSLOT + 8;
+// extra shared memory of the fold_dg variant: the per-row dg bank [64][128] and the
+// per-(sub-block, channel) totals, double-buffered by unit parity
+constexpr int SM_FOLD_BANK = (SM_TOTAL + 127) / 128 * 128;
+constexpr int SM_FOLD_TOT = SM_FOLD_BANK + BT * KD * 4;
+constexpr int SM_TOTAL_FOLD = SM_FOLD_TOT + 2 * NBLK * KD * 4;
 static_assert(STAGE_BYTES % 128 == 0, "TMA destinations need 128-byte alignment");
 static_assert(ST_DQ % 1024 == 0 && ST_DK % 1024 == 0, "dA tiles alignment");
 
@@ -95,6 +100,21 @@ struct TmaMaps {
     CUtensorMap q, k, g, daqk, dakk;
 };
 
+// Options of the extended entry point.  H in the kernel is the number of heads of g,
+// beta, dA and the outputs (HV); q and k have HV / G heads.
+struct Extras {
+    const float *dq_in, *dk_in, *dg_in, *db_in;  // added in-kernel when non-null
+    int G;  // value heads per q/k head
+};
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) {
+    return __float2half_rn(x);
+}
+
 __device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
     uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(gmem) : "memory");
@@ -105,13 +125,13 @@ __device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
 // tensor map can describe it when H is not a multiple of 4).
 __device__ __forceinline__ void load_unit(unsigned char *st, uint64_t *full,
                                           const TmaMaps &tm, const float *__restrict__ beta,
-                                          long long u, int T, int H, int lane) {
+                                          long long u, int T, int H, int G, int lane) {
     const Unit x = decode_unit(u, H, T / BT);
     const int row = x.b * T + x.c * BT;  // first token row of the unit
     if (lane == 0) {
         tc::mbar_arrive_expect_tx(full, STAGE_TX_BYTES);
-        tc::tma_load_3d(st + ST_Q, &tm.q, 0, x.h, row, full);
-        tc::tma_load_3d(st + ST_K, &tm.k, 0, x.h, row, full);
+        tc::tma_load_3d(st + ST_Q, &tm.q, 0, x.h / G, row, full);
+        tc::tma_load_3d(st + ST_K, &tm.k, 0, x.h / G, row, full);
         tc::tma_load_3d(st + ST_G, &tm.g, 0, x.h, row, full);
 #pragma unroll
         for (int t = 0; t < NBLK; ++t) {
@@ -134,12 +154,15 @@ __device__ __forceinline__ void load_unit(unsigned char *st, uint64_t *full,
     tc::cp_async_mbar_arrive_noinc(full);
 }
 
-template <typename io_t>
+// ACCUM: add the optional incoming gradients of Extras; FOLD: return dg as its
+// inclusive reverse cumsum inside each chunk; EMIT: store dq and dk as io_t.
+template <typename io_t, bool ACCUM, bool FOLD, bool EMIT>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restrict__ beta,
-                        float *__restrict__ dq, float *__restrict__ dk,
-                        float *__restrict__ db, float *__restrict__ dg, int T, int H,
-                        long long units) {
+                        void *dq_out, void *dk_out, float *db, float *dg, int T, int H,
+                        long long units, const Extras ex) {
+    float *dq = reinterpret_cast<float *>(dq_out);
+    float *dk = reinterpret_cast<float *>(dk_out);
     extern __shared__ __align__(1024) unsigned char smem[];
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -176,9 +199,9 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
 
     if (warp == 0) {  // the first two units of this CTA
         const long long u0 = blockIdx.x;
-        if (u0 < units) load_unit(smem, &full[0], tm, beta, u0, T, H, lane);
+        if (u0 < units) load_unit(smem, &full[0], tm, beta, u0, T, H, ex.G, lane);
         if (u0 + stride < units)
-            load_unit(smem + STAGE_BYTES, &full[1], tm, beta, u0 + stride, T, H, lane);
+            load_unit(smem + STAGE_BYTES, &full[1], tm, beta, u0 + stride, T, H, ex.G, lane);
     }
 
     bool ok = true;
@@ -378,15 +401,44 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
                 dkt2[r >> 1].x = fmaf(aqd, qv, dkt2[r >> 1].x);
             }
         };
+        // incoming gradients (ACCUM): fetched three output rows ahead of their use
+        float inq[BC], ink[BC], ing[BC];
+        auto fetch_in = [&](const int r) {
+            if constexpr (ACCUM) {
+                const size_t off = obase + (size_t)((uint32_t)r * hk);
+                inq[r] = ex.dq_in ? __ldg(ex.dq_in + off) : 0.f;
+                ink[r] = ex.dk_in ? __ldg(ex.dk_in + off) : 0.f;
+                ing[r] = ex.dg_in ? __ldg(ex.dg_in + off) : 0.f;
+            }
+        };
+        float fold_run = 0.f;  // FOLD: running suffix sum of dg inside the sub-block
+        float *bank = reinterpret_cast<float *>(smem + SM_FOLD_BANK);
         auto out_row = [&](const int r) {
             const int row = r0 + r;
             const size_t off = obase + (size_t)((uint32_t)r * hk);
+            if (r >= 3) fetch_in(r - 3);
             const float qv = to_f32(sq[row * KD + d]);
             const float kv = KDA_EL(k2, r), dkv = KDA_EL(dkt2, r);
             const float pk = sbeta[row] * acck[r];
-            dq[off] = accq[r];
-            dk[off] = pk + dkv;
-            dg[off] = LN2 * fmaf(qv, accq[r], (pk - dkv) * kv);
+            float vq = accq[r], vk = pk + dkv, vg = LN2 * fmaf(qv, accq[r], (pk - dkv) * kv);
+            if constexpr (ACCUM) {
+                vq += inq[r];
+                vk += ink[r];
+                vg += ing[r];
+            }
+            if constexpr (EMIT) {
+                reinterpret_cast<io_t *>(dq_out)[off] = from_f32<io_t>(vq);
+                reinterpret_cast<io_t *>(dk_out)[off] = from_f32<io_t>(vk);
+            } else {
+                dq[off] = vq;
+                dk[off] = vk;
+            }
+            if constexpr (FOLD) {
+                fold_run += vg;
+                bank[row * KD + d] = fold_run;
+            } else {
+                dg[off] = vg;
+            }
             dbv[r] = acck[r] * kv;
         };
         // db[r] = sum over d of 8 rows at a time: transpose-reduce across the warp's lanes
@@ -410,6 +462,9 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             if ((lane & 3) == 0) sdbp[(warp & 3) * BT + r0 + rbase + (lane >> 2)] = v[0];
         };
 
+        fetch_in(BC - 1);
+        fetch_in(BC - 2);
+        fetch_in(BC - 3);
 #pragma unroll
         for (int r = BC - 1; r >= BC / 2; --r) {
             accq[r] = acck[r] = 0.f;
@@ -479,8 +534,27 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         tc::named_bar_sync(1 + i, 128);
         if ((warp & 3) == 0 && lane < BC) {
             const int row = r0 + lane;
-            db[grow(un, row, T, H)] = (sdbp[row] + sdbp[BT + row]) +
-                                      (sdbp[2 * BT + row] + sdbp[3 * BT + row]);
+            const size_t brow = grow(un, row, T, H);
+            float v = (sdbp[row] + sdbp[BT + row]) + (sdbp[2 * BT + row] + sdbp[3 * BT + row]);
+            if constexpr (ACCUM) {
+                if (ex.db_in) v += ex.db_in[brow];
+            }
+            db[brow] = v;
+        }
+        if constexpr (FOLD) {
+            // the four threads of channel d (one per sub-block, in warps c, c+4, c+8,
+            // c+12) exchange their sub-block totals; each adds the totals of the later
+            // sub-blocks to its banked in-block suffix sums
+            float *tot = reinterpret_cast<float *>(smem + SM_FOLD_TOT) + (it & 1) * NBLK * KD;
+            tot[i * KD + d] = fold_run;
+            tc::named_bar_sync(5 + (warp & 3), 128);
+            float later = 0.f;
+#pragma unroll
+            for (int j = NBLK - 1; j > 0; --j)
+                if (j > i) later += tot[j * KD + d];
+#pragma unroll
+            for (int r = 0; r < BC; ++r)
+                dg[obase + (size_t)((uint32_t)r * hk)] = bank[(r0 + r) * KD + d] + later;
         }
 
         // ---- unit done: the last warp releases the stage and refills it ----
@@ -491,7 +565,7 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         prev = __shfl_sync(0xffffffffu, prev, 0);
         if ((prev % TC_WARPS) == TC_WARPS - 1 && u + 2 * stride < units) {
             tc::fence_proxy_async_smem();
-            load_unit(st, &full[sidx], tm, beta, u + 2 * stride, T, H, lane);
+            load_unit(st, &full[sidx], tm, beta, u + 2 * stride, T, H, ex.G, lane);
         }
     }
 
@@ -533,12 +607,13 @@ cudaError_t encode(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void 
 cudaError_t make_maps(const BwdArgs &a, TmaMaps *tm) {
     cudaError_t e = get_encoder();
     if (e != cudaSuccess) return e;
-    const cuuint64_t rows = (cuuint64_t)a.B * a.T, H = (cuuint64_t)a.H;
+    const cuuint64_t rows = (cuuint64_t)a.B * a.T, HQ = (cuuint64_t)a.H;
+    const cuuint64_t H = (cuuint64_t)(a.HV > 0 ? a.HV : a.H);
     const CUtensorMapDataType io =
         a.fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     {  // q, k: (channel, head, token row); one unit = box (128, 1, 64)
-        const cuuint64_t dims[3] = {KD, H, rows};
-        const cuuint64_t str[2] = {KD * 2, H * KD * 2};
+        const cuuint64_t dims[3] = {KD, HQ, rows};
+        const cuuint64_t str[2] = {KD * 2, HQ * KD * 2};
         const cuuint32_t box[3] = {KD, 1, BT};
         if ((e = encode(&tm->q, io, 3, a.q, dims, str, box)) != cudaSuccess) return e;
         if ((e = encode(&tm->k, io, 3, a.k, dims, str, box)) != cudaSuccess) return e;
@@ -568,11 +643,12 @@ cudaError_t make_maps(const BwdArgs &a, TmaMaps *tm) {
     return cudaSuccess;
 }
 
-template <typename io_t>
+template <typename io_t, bool ACCUM, bool FOLD, bool EMIT>
 cudaError_t launch_typed(const BwdArgs &a, cudaStream_t stream) {
-    auto kern = kda_intra_bwd_tc_kernel<io_t>;
+    auto kern = kda_intra_bwd_tc_kernel<io_t, ACCUM, FOLD, EMIT>;
+    const int smem_bytes = FOLD ? SM_TOTAL_FOLD : SM_TOTAL;
     cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM_TOTAL);
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -584,17 +660,39 @@ cudaError_t launch_typed(const BwdArgs &a, cudaStream_t stream) {
     }
     TmaMaps tm;
     if ((e = make_maps(a, &tm)) != cudaSuccess) return e;
-    const long long units = (long long)a.B * a.H * (a.T / BT);
+    const int HV = a.HV > 0 ? a.HV : a.H;
+    Extras ex;
+    ex.dq_in = a.dq_in;
+    ex.dk_in = a.dk_in;
+    ex.dg_in = a.dg_in;
+    ex.db_in = a.db_in;
+    ex.G = HV / a.H;
+    const long long units = (long long)a.B * HV * (a.T / BT);
     const unsigned grid = (unsigned)(units < nsm ? units : nsm);
-    kern<<<grid, TC_THREADS, SM_TOTAL, stream>>>(tm, a.beta, a.dq, a.dk, a.db, a.dg, a.T, a.H,
-                                                 units);
+    kern<<<grid, TC_THREADS, smem_bytes, stream>>>(tm, a.beta, a.dq, a.dk, a.db, a.dg, a.T, HV,
+                                                   units, ex);
     return cudaGetLastError();
+}
+
+template <typename io_t, bool EMIT>
+cudaError_t launch_opts(const BwdArgs &a, cudaStream_t stream) {
+    const bool accum = a.dq_in || a.dk_in || a.dg_in || a.db_in;
+    if (accum)
+        return a.fold_dg ? launch_typed<io_t, true, true, EMIT>(a, stream)
+                         : launch_typed<io_t, true, false, EMIT>(a, stream);
+    return a.fold_dg ? launch_typed<io_t, false, true, EMIT>(a, stream)
+                     : launch_typed<io_t, false, false, EMIT>(a, stream);
+}
+
+template <typename io_t>
+cudaError_t launch_io(const BwdArgs &a, cudaStream_t stream) {
+    return a.emit_io ? launch_opts<io_t, true>(a, stream) : launch_opts<io_t, false>(a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_intra_tc(const BwdArgs &a, cudaStream_t stream) {
-    return a.fp16 ? launch_typed<__half>(a, stream) : launch_typed<__nv_bfloat16>(a, stream);
+    return a.fp16 ? launch_io<__half>(a, stream) : launch_io<__nv_bfloat16>(a, stream);
 }
 
 }  // namespace kda

@@ -8,9 +8,15 @@ namespace kda {
 struct BwdArgs {
     const void *q, *k;
     const float *g, *beta, *dAqk, *dAkk;
-    float *dq, *dk, *db, *dg;
-    int B, T, H;
-    bool fp16;  // q/k element type: false = bf16, true = fp16
+    void *dq, *dk;  // fp32, or the q/k element type when emit_io is set
+    float *db, *dg;
+    int B, T, H;    // H = heads of q and k
+    bool fp16;      // q/k element type: false = bf16, true = fp16
+    // extended options (tensor-core path only)
+    int HV = 0;     // heads of g, beta, dA and every output (0 = H); a multiple of H
+    const float *dq_in = nullptr, *dk_in = nullptr, *dg_in = nullptr, *db_in = nullptr;
+    bool fold_dg = false;  // dg as its inclusive reverse cumsum inside each chunk
+    bool emit_io = false;  // dq, dk written in the q/k element type
 };
 
 // All-FP32 SIMT kernel (one CTA per unit).

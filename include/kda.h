@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 1
+#define KDA_ABI_VERSION 2
 #define KDA_BT 64  /* chunk length */
 #define KDA_BC 16  /* sub-block length inside a chunk */
 #define KDA_K 128  /* head dimension */
@@ -76,7 +76,8 @@ typedef enum {
     KDA_ERR_CUDA = 5,               /* a CUDA runtime call or the launch failed */
     KDA_ERR_UNSUPPORTED_DEVICE = 6, /* current device is not compute capability 10.3 */
     KDA_ERR_OVERLAP = 7,            /* two argument buffers overlap */
-    KDA_ERR_WORKSPACE = 8           /* workspace missing or too small (*_host only) */
+    KDA_ERR_WORKSPACE = 8,          /* workspace missing or too small (*_host only) */
+    KDA_ERR_OPTION = 9              /* unsupported option combination (*_ex only) */
 } kda_status_t;
 
 typedef enum { KDA_BF16 = 0, KDA_FP16 = 1 } kda_dtype_t;
@@ -122,6 +123,44 @@ kda_status_t kda_intra_bwd_host(const void *q, const void *k, const float *g,
                                 int B, int T, int H, kda_dtype_t qk_dtype,
                                 void *workspace, size_t workspace_bytes,
                                 kda_stream_t stream);
+
+/*
+ * Options of kda_intra_bwd_ex.  Zero-initialise, then set what you need; a zeroed
+ * struct (or a NULL pointer) gives exactly kda_intra_bwd.  These follow the bwd_intra
+ * page's host wrapper and kernel options (its incoming-gradient tensors, fold_dg,
+ * emit_bf16 and gva group size).
+ *
+ *   HV             heads of g, beta, dAqk, dAkk and of every output and *_in tensor;
+ *                  q and k keep H heads and value head hv reads q/k head hv / (HV / H)
+ *                  (grouped value attention).  0 means HV = H.  Must be a multiple of H.
+ *   dq_in, dk_in,  optional [B,T,HV,128] fp32 gradients added in-kernel to dq, dk, dg
+ *   dg_in          (NULL = none).  May be the same pointer as the matching output
+ *                  (in-place accumulation); any other overlap is rejected.
+ *   db_in          optional [B,T,HV] fp32 added to db; may equal db.
+ *   fold_dg        1: dg comes back as its inclusive reverse cumsum inside each
+ *                  64-token chunk, out[t] = sum_{t' >= t in t's chunk} dg[t'] (the
+ *                  per-step gate's gradient; dg_in is added before the fold).
+ *   dqdk_io_dtype  1: dq and dk are written in qk_dtype (round to nearest) instead of
+ *                  fp32 -- bitwise the cast of the fp32 result.  Not allowed with HV > H
+ *                  (the grouped-head reduction that follows must see fp32 values).
+ *
+ * Runs on the tensor-core path (the same accuracy contract as kda_intra_bwd).
+ */
+typedef struct {
+    int HV;
+    const float *dq_in;
+    const float *dk_in;
+    const float *dg_in;
+    const float *db_in;
+    int fold_dg;
+    int dqdk_io_dtype;
+} kda_intra_bwd_opts_t;
+
+kda_status_t kda_intra_bwd_ex(const void *q, const void *k, const float *g,
+                              const float *beta, const float *dAqk, const float *dAkk,
+                              void *dq, void *dk, float *db, float *dg,
+                              int B, int T, int H, kda_dtype_t qk_dtype,
+                              const kda_intra_bwd_opts_t *opts, kda_stream_t stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *kda_status_str(kda_status_t status);

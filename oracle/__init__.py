@@ -110,3 +110,45 @@ def intra_bwd(q, k, g, beta, dAqk, dAkk, *, bt: int = 64, nthreads: int = 0, lib
     if rc:
         raise ValueError("oracle backward rejected its arguments")
     return dq, dk, db, dg
+
+
+def chunk_reverse_cumsum(x, bt: int = 64) -> np.ndarray:
+    """Inclusive reverse cumsum along tokens inside each chunk of bt tokens:
+    out[t] = sum of x[t'] over t' >= t in t's chunk (axis 1 of a [B, T, ...] array)."""
+    x = _f64(x)
+    B, T = x.shape[:2]
+    y = x.reshape(B, T // bt, bt, *x.shape[2:])
+    y = np.flip(np.cumsum(np.flip(y, axis=2), axis=2), axis=2)
+    return np.ascontiguousarray(y.reshape(x.shape))
+
+
+def intra_bwd_ex(q, k, g, beta, dAqk, dAkk, *, dq_in=None, dk_in=None, dg_in=None,
+                 db_in=None, fold_dg=False, bt: int = 64, nthreads: int = 0, lib=None):
+    """The extended contract, composed from intra_bwd:
+
+    * grouped value heads: q, k have H heads, the rest HV = g.shape[2]; value head hv
+      uses q/k head hv // (HV // H), so the per-value-head problem is intra_bwd on q/k
+      with every head repeated HV // H times;
+    * incoming gradients are added to the outputs;
+    * fold_dg replaces dg (incoming part included) by its chunk-local reverse cumsum.
+    """
+    q, k = _f64(q), _f64(k)
+    HV, H = _f64(g).shape[2], q.shape[2]
+    if HV % H:
+        raise ValueError("HV must be a multiple of H")
+    G = HV // H
+    if G > 1:
+        q = np.repeat(q, G, axis=2)
+        k = np.repeat(k, G, axis=2)
+    dq, dk, db, dg = intra_bwd(q, k, g, beta, dAqk, dAkk, bt=bt, nthreads=nthreads, lib=lib)
+    if dq_in is not None:
+        dq = dq + _f64(dq_in)
+    if dk_in is not None:
+        dk = dk + _f64(dk_in)
+    if db_in is not None:
+        db = db + _f64(db_in)
+    if dg_in is not None:
+        dg = dg + _f64(dg_in)
+    if fold_dg:
+        dg = chunk_reverse_cumsum(dg, bt)
+    return dq, dk, db, dg

@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for want in ("kda_intra_bwd", "kda_intra_bwd_fp32", "kda_intra_bwd_host",
                  "kda_intra_bwd_host_workspace_bytes", "kda_status_str",
-                 "kda_abi_version"):
+                 "kda_abi_version", "kda_intra_bwd_ex"):
         assert want in names
 
 
@@ -47,7 +47,7 @@ def test_abi_version(lib):
 
 
 def test_status_strings(lib):
-    for code in range(9):
+    for code in range(10):
         s = kda.kda_status_str(code)
         assert s.startswith("KDA_")
     assert kda.kda_status_str(99) == "KDA_ERR_UNKNOWN"
@@ -142,3 +142,43 @@ def test_python_binding_refuses_cpu_tensors():
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="no fallback"):
         kda.load_library(str(tmp_path / "libkda.so"))
+
+
+# ---------------------------------------------------------------- kda_intra_bwd_ex
+
+def ex_call(lib, B=1, T=64, H=1, dtype=0, HV=0, fold=0, emit=0, ins=None, **override):
+    args = fake_args(B, T, H, dtype, **override)[:-1]
+    opts = kda.KdaOpts()
+    opts.HV = HV
+    opts.fold_dg = fold
+    opts.dqdk_io_dtype = emit
+    for name, val in (ins or {}).items():
+        setattr(opts, name, val)
+    return lib.kda_intra_bwd_ex(*args, ctypes.byref(opts), ctypes.c_void_p(0))
+
+
+def test_ex_rejections(lib):
+    assert ex_call(lib, H=2, HV=3) == ERR_SHAPE              # HV not a multiple of H
+    assert ex_call(lib, H=2, HV=-2) == ERR_SHAPE
+    assert ex_call(lib, H=1, HV=2, emit=1) == 9               # io-dtype outputs with GVA
+    assert ex_call(lib, fold=2) == 9
+    assert ex_call(lib, emit=3) == 9
+    assert ex_call(lib, ins={"dq_in": BASE + 11 * SPAN + 2}) == ERR_ALIGN
+    # an incoming gradient overlapping an output other than its own
+    assert ex_call(lib, ins={"dk_in": BASE + 6 * SPAN}) == ERR_OVERLAP
+    # partial overlap with its own output
+    assert ex_call(lib, ins={"dq_in": BASE + 6 * SPAN + 64}) == ERR_OVERLAP
+    assert ex_call(lib, q=0) == ERR_NULL
+
+
+def test_ex_accepts_in_place_and_reaches_the_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("would launch on a real device")
+    ins = {"dq_in": BASE + 6 * SPAN, "dk_in": BASE + 7 * SPAN, "db_in": BASE + 8 * SPAN,
+           "dg_in": BASE + 9 * SPAN}
+    assert ex_call(lib, H=2, HV=4, fold=1, ins=ins) in (ERR_CUDA, ERR_DEVICE)
+    assert ex_call(lib, emit=1) in (ERR_CUDA, ERR_DEVICE)
+    # NULL options behave like kda_intra_bwd
+    args = fake_args()[:-1]
+    assert lib.kda_intra_bwd_ex(*args, None, ctypes.c_void_p(0)) in (ERR_CUDA, ERR_DEVICE)

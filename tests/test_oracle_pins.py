@@ -81,3 +81,57 @@ def test_rejects_bad_shapes(lib):
     args = [inp[n] for n in ("q", "k", "g", "beta", "dAqk", "dAkk")]
     with pytest.raises(ValueError):
         oracle.intra_bwd(*args, bt=5, lib=lib)  # T % bt != 0
+
+
+# ---------------------------------------------------------------- extended contract
+
+def test_chunk_reverse_cumsum_pins():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((2, 24, 3, 5))
+    y = oracle.chunk_reverse_cumsum(x, bt=8)
+    for c in range(3):
+        sl = slice(8 * c, 8 * c + 8)
+        xc, yc = x[:, sl], y[:, sl]
+        assert np.allclose(yc[:, -1], xc[:, -1], rtol=0, atol=0)          # last row
+        assert np.allclose(yc[:, :-1] - yc[:, 1:], xc[:, :-1], atol=1e-14)  # differences
+        assert np.allclose(yc[:, 0], xc.sum(axis=1), atol=1e-13)           # first row
+
+
+def test_grouped_heads_pinned_by_finite_differences():
+    """With q/k shared by G value heads, the sum of the per-value-head dq (dk) over a
+    group is dL/d(shared q) (dk), by central differences of the summed loss."""
+    B, T, H, G, K, bt = 1, 16, 1, 3, 3, 8
+    rng = np.random.default_rng(17)
+    base = _pins.tiny_inputs(B, T, H * G, K, bt, seed=17)
+    q = rng.standard_normal((B, T, H, K))
+    k = rng.standard_normal((B, T, H, K))
+    lib = oracle.load()
+
+    def loss(qq, kk):
+        qx, kx = np.repeat(qq, G, axis=2), np.repeat(kk, G, axis=2)
+        Aqk, Akk = oracle.intra_fwd(qx, kx, base["g"], base["beta"], bt=bt, lib=lib)
+        return float(np.sum(base["dAqk"] * Aqk) + np.sum(base["dAkk"] * Akk))
+
+    dq, dk, _, _ = oracle.intra_bwd_ex(q, k, base["g"], base["beta"], base["dAqk"],
+                                       base["dAkk"], bt=bt, lib=lib)
+    for name, x, grad in (("q", q, dq), ("k", k, dk)):
+        shared = grad.reshape(B, T, H, G, K).sum(axis=3)
+        fd = np.zeros_like(x)
+        h = 1e-6
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + h
+            lp = loss(q, k)
+            x[idx] = old - h
+            lm = loss(q, k)
+            x[idx] = old
+            fd[idx] = (lp - lm) / (2 * h)
+        assert _pins.rel_err(shared, fd) < 1e-6, name
+
+
+def test_grouped_heads_with_one_group_is_the_plain_backward():
+    inp = _pins.tiny_inputs(1, 16, 2, 4, 8, seed=21)
+    a = oracle.intra_bwd(*(inp[n] for n in ("q", "k", "g", "beta", "dAqk", "dAkk")), bt=8)
+    b = oracle.intra_bwd_ex(*(inp[n] for n in ("q", "k", "g", "beta", "dAqk", "dAkk")), bt=8)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
