@@ -62,7 +62,7 @@ def algorithmic_bytes_per_unit(qk_bytes: int = 2, group: int = 1, accumulate: bo
 
 
 KERNEL_SOURCES = {
-    "kda_intra_bwd_tc_kernel": ("kda_intra_tc.cu", "tc_ptx.cuh", "kda_common.cuh"),
+    "kda_intra_bwd_tc_kernel": ("kda_intra_tc.cuh", "kda_intra_tc.cu", "tc_ptx.cuh", "kda_common.cuh"),
     "kda_intra_bwd_fp32_kernel": ("kda_intra_fp32.cu", "kda_common.cuh"),
 }
 

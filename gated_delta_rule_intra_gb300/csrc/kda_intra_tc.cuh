@@ -1,0 +1,629 @@
+// Tensor-core kernel for the KDA intra-chunk backward (sm_103a, tcgen05 + TMEM + TMA).
+//
+// Persistent grid, one 512-thread CTA per SM, units (b, h, 64-token chunk) dealt
+// round-robin.  Two shared-memory stages hold the inputs of consecutive units; the
+// tensor memory accelerator fills a stage while the other one is being computed.
+// There is no CTA-wide barrier inside the unit loop: warps hand work to each other
+// through mbarriers and two shared counters, so fast warps run ahead into the
+// next unit instead of idling:
+//   * the stage-full mbarrier completes when a unit's TMA tiles and beta have landed;
+//   * the last warp to finish writing its tensor-core operands issues the unit's 36
+//     MMAs (every other warp goes straight on to the diagonal blocks);
+//   * the last warp to finish a unit releases its stage and loads the unit after
+//     next into it;
+//   * the per-row sum for dbeta meets across the four warps of a sub-block at a
+//     128-thread named barrier.
+//
+// Thread (i, d) owns sub-block i (rows 16i..16i+15) at channel d; its TMEM lane is d
+// (warp w reaches lanes 32(w%4)..32(w%4)+31, and d = 32(w%4) + lane).
+//
+// Cross-sub-block terms (bwd_intra page, module docstring): for r in block t and
+// s in block j < t,
+//     2^(g_r - g_s) = 2^(g_r - g_b0(t)) * 2^(g_b0(t) - g_e(j)) * 2^(g_e(j) - g_s)
+// with b0(t) = 16t and e(j) = 16(j+1); every exponent is <= 0.  The last two
+// factors are folded into a TF32 operand per target block t,
+//     A_t[d, s] = k[s,d] 2^(g_16t - g_s)   (s < 16t),
+// kept in TMEM and multiplied on the tensor core by the dA rows of block t:
+//     Xq_t[d, n] = sum_s A_t[d, s] dAqk[16t+n, s]   (same for Xk_t with dAkk)
+// and the first factor is applied on the TMEM->register path.  The column side
+// uses the mirrored split through the source block's end boundary:
+//     P_j[d, s] = sum_{r in blk j} q[r,d] 2^(g_r - g_16j) dAqk[r,s]
+//               + beta_r k[r,d] 2^(g_r - g_16j) dAkk[r,s]        (s < 16j)
+//     dkt_cross[s,d] = 2^(g_e(i) - g_s) * sum_{j>i} 2^(g_16j - g_e(i)) P_j[d, s].
+// The 16x16 diagonal blocks run on the FP32 pipes with one exp2 per (r, s, d),
+// two source rows at a time in packed FP32x2 arithmetic.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kda_common.cuh"
+#include "kda_launch.h"
+#include "tc_ptx.cuh"
+
+namespace kda {
+namespace tcimpl {
+
+constexpr int TC_THREADS = 512;
+constexpr int TC_WARPS = TC_THREADS / 32;
+
+// ---- shared memory: two input stages + single-buffered derived operands ----
+// dA tiles: the ten lower 16x16 blocks (t, j <= t) of a unit, block (t, j) at
+// dablk(t, j) KB, each in the K-major core-matrix layout of a tensor-core operand:
+// element (n, k) (n = row in block t, k = column in block j) at byte
+//     (k/4)*256 + (n/8)*128 + (n%8)*16 + (k%4)*4.
+// Blocks (t, 0..t-1) are contiguous, so they form the B operand of target t
+// (N = 16 rows, K = 16t, core matrices 256 B apart along K and 128 B along N).
+constexpr int ST_Q = 0;                      // io_t [64][128]
+constexpr int ST_K = ST_Q + BT * KD * 2;     // io_t [64][128]
+constexpr int ST_G = ST_K + BT * KD * 2;     // f32  [64][128]
+constexpr int ST_DQ = ST_G + BT * KD * 4;    // dAqk: 10 blocks x 1 KB
+constexpr int ST_DK = ST_DQ + 10 * 1024;     // dAkk
+constexpr int ST_BETA = ST_DK + 10 * 1024;   // f32 [64]
+constexpr int STAGE_BYTES = ST_BETA + 256;   // 86272
+constexpr int SM_BCQ = 2 * STAGE_BYTES;      // dAqk blocks of target j transposed (K-major)
+constexpr int SM_BCK = SM_BCQ + 6144;
+constexpr int SM_DBP = SM_BCK + 6144;        // db partials f32 [4][64]
+constexpr int SM_FULL = SM_DBP + 1024;       // 2 stage-full mbarriers
+constexpr int SM_MMA = SM_FULL + 16;         // MMAs-done mbarrier
+constexpr int SM_CNT = SM_MMA + 8;           // operand counter, unit-done counter
+constexpr int SM_TSLOT = SM_CNT + 8;
+constexpr int SM_TOTAL = SM_TSLOT + 8;
+// extra shared memory of the fold_dg variant: the per-row dg bank [64][128] and the
+// per-(sub-block, channel) totals, double-buffered by unit parity
+constexpr int SM_FOLD_BANK = (SM_TOTAL + 127) / 128 * 128;
+constexpr int SM_FOLD_TOT = SM_FOLD_BANK + BT * KD * 4;
+constexpr int SM_TOTAL_FOLD = SM_FOLD_TOT + 2 * NBLK * KD * 4;
+static_assert(STAGE_BYTES % 128 == 0, "TMA destinations need 128-byte alignment");
+static_assert(ST_DQ % 1024 == 0 && ST_DK % 1024 == 0, "dA tiles alignment");
+
+constexpr uint32_t STAGE_TX_BYTES = 2 * BT * KD * 2 + BT * KD * 4 + 2 * 10 * 1024;
+constexpr uint32_t FULL_ARRIVALS = 1 + 32;  // expect_tx by lane 0 + beta copies by 32 lanes
+
+__host__ __device__ constexpr int dablk(int t, int j) { return t * (t + 1) / 2 + j; }
+
+// byte offset of target j's transposed operand inside a 6 KB region: 1, 2, 3 KB
+__device__ __forceinline__ uint32_t bcol_off(int j) { return 512u * (uint32_t)((j - 1) * j); }
+
+// ---- TMEM column map (512 columns, fp32) ----
+__device__ __forceinline__ uint32_t tm_arow(int t) { return 8u * (uint32_t)(t * (t - 1)); }  // A_t: 16t cols
+constexpr uint32_t TM_AQB = 96;    // q_r 2^(g_r - g_16j), column r-16  (48 cols)
+constexpr uint32_t TM_AKBB = 144;  // beta_r k_r 2^(g_r - g_16j)          (48 cols)
+constexpr uint32_t TM_XQ = 192;    // Xq_t at +16(t-1)                     (48 cols)
+constexpr uint32_t TM_XK = 240;    // Xk_t                                   (48 cols)
+__device__ __forceinline__ uint32_t tm_p(int j) { return 288u + 8u * (uint32_t)(j * (j - 1)); }
+constexpr uint32_t TM_FB = 384;    // 2^(g_r - g_16i) for block i >= 1 at +16(i-1)
+constexpr uint32_t TM_FA = 432;    // 2^(g_16(i+1) - g_s) for block i <= 2 at +16i
+constexpr uint32_t TM_COLS = 512;
+
+constexpr uint32_t SPIN_LIMIT = 1u << 22;
+
+struct TmaMaps {
+    CUtensorMap q, k, g, daqk, dakk;
+};
+
+// Options of the extended entry point.  H in the kernel is the number of heads of g,
+// beta, dA and the outputs (HV); q and k have HV / G heads.
+struct Extras {
+    const float *dq_in, *dk_in, *dg_in, *db_in;  // added in-kernel when non-null
+    int G;  // value heads per q/k head
+};
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) {
+    return __float2half_rn(x);
+}
+
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
+    uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(gmem) : "memory");
+}
+
+// One warp queues every copy of one unit into a stage: 23 TMA tiles from lane 0,
+// beta as 64 four-byte copies from all lanes (its rows are H floats apart, so no
+// tensor map can describe it when H is not a multiple of 4).
+__device__ __forceinline__ void load_unit(unsigned char *st, uint64_t *full,
+                                          const TmaMaps &tm, const float *__restrict__ beta,
+                                          long long u, int T, int H, int G, int lane) {
+    const Unit x = decode_unit(u, H, T / BT);
+    const int row = x.b * T + x.c * BT;  // first token row of the unit
+    if (lane == 0) {
+        tc::mbar_arrive_expect_tx(full, STAGE_TX_BYTES);
+        tc::tma_load_3d(st + ST_Q, &tm.q, 0, x.h / G, row, full);
+        tc::tma_load_3d(st + ST_K, &tm.k, 0, x.h / G, row, full);
+        tc::tma_load_3d(st + ST_G, &tm.g, 0, x.h, row, full);
+#pragma unroll
+        for (int t = 0; t < NBLK; ++t) {
+#pragma unroll
+            for (int j = 0; j <= t; ++j) {
+                const int rg = (row + BC * t) >> 3;
+                tc::tma_load_5d(st + ST_DQ + dablk(t, j) * 1024, &tm.daqk, 0, 0, rg, 4 * j, x.h,
+                                full);
+                tc::tma_load_5d(st + ST_DK + dablk(t, j) * 1024, &tm.dakk, 0, 0, rg, 4 * j, x.h,
+                                full);
+            }
+        }
+    }
+    const size_t b0 = grow(x, 0, T, H);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int r = lane + 32 * e;
+        cp_async4(st + ST_BETA + r * 4, beta + b0 + (size_t)r * H);
+    }
+    tc::cp_async_mbar_arrive_noinc(full);
+}
+
+// ACCUM: add the optional incoming gradients of Extras; FOLD: return dg as its
+// inclusive reverse cumsum inside each chunk; EMIT: store dq and dk as io_t.
+template <typename io_t, bool ACCUM, bool FOLD, bool EMIT>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restrict__ beta,
+                        void *dq_out, void *dk_out, float *db, float *dg, int T, int H,
+                        long long units, const Extras ex) {
+    float *dq = reinterpret_cast<float *>(dq_out);
+    float *dk = reinterpret_cast<float *>(dk_out);
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int i = tid >> 7;  // sub-block, warp-uniform
+    const int d = tid & 127;
+    const int r0 = i * BC;
+    const int NT = T / BT;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM_FULL);
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + SM_MMA);
+    uint32_t *ops_count = reinterpret_cast<uint32_t *>(smem + SM_CNT);
+    uint32_t *done_count = ops_count + 1;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + SM_TSLOT);
+    float *sdbp = reinterpret_cast<float *>(smem + SM_DBP);
+    const long long stride = gridDim.x;
+
+    if (warp == 0) tc::tmem_alloc(tslot, TM_COLS);
+    if (tid == 0) {
+        tc::mbar_init(&full[0], FULL_ARRIVALS);
+        tc::mbar_init(&full[1], FULL_ARRIVALS);
+        tc::mbar_init(mbar, 1);
+        ops_count[0] = 0u;
+        done_count[0] = 0u;
+        tc::prefetch_tmap(&tm.q);
+        tc::prefetch_tmap(&tm.k);
+        tc::prefetch_tmap(&tm.g);
+        tc::prefetch_tmap(&tm.daqk);
+        tc::prefetch_tmap(&tm.dakk);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tbase = *tslot;
+    const uint32_t tlane = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
+
+    if (warp == 0) {  // the first two units of this CTA
+        const long long u0 = blockIdx.x;
+        if (u0 < units) load_unit(smem, &full[0], tm, beta, u0, T, H, ex.G, lane);
+        if (u0 + stride < units)
+            load_unit(smem + STAGE_BYTES, &full[1], tm, beta, u0 + stride, T, H, ex.G, lane);
+    }
+
+    bool ok = true;
+    int it = 0;
+    for (long long u = blockIdx.x; u < units; u += stride, ++it) {
+        const int sidx = it & 1;
+        unsigned char *st = smem + sidx * STAGE_BYTES;
+        ok &= tc::mbar_wait(&full[sidx], (uint32_t)(it >> 1) & 1u, SPIN_LIMIT);
+
+        const float *sg = reinterpret_cast<const float *>(st + ST_G);
+        const io_t *sq = reinterpret_cast<const io_t *>(st + ST_Q);
+        const io_t *sk = reinterpret_cast<const io_t *>(st + ST_K);
+        const float *sbeta = reinterpret_cast<const float *>(st + ST_BETA);
+
+        // ---- column-side B operands: dA blocks (j, 0..j-1) transposed.  The loads go
+        // out first so their latency overlaps the column loads and the prescale. ----
+        float trq[3], trk[3];
+        int trdst[3];
+        {
+            const float *aq = reinterpret_cast<const float *>(st + ST_DQ);
+            const float *ak = reinterpret_cast<const float *>(st + ST_DK);
+#pragma unroll
+            for (int x = 0; x < 3; ++x) {
+                const int idx = tid + x * TC_THREADS;  // < 1536
+                const int j = idx >= 768 ? 3 : idx >= 256 ? 2 : 1;
+                const int e = idx - 128 * j * (j - 1);
+                // e enumerates the destination floats in order (n/8, k/4, n%8, k%4)
+                const int n = (e >> 7) * 8 + ((e >> 2) & 7);  // s
+                const int kk = ((e >> 5) & 3) * 4 + (e & 3);  // r - 16j
+                const int src = dablk(j, n >> 4) * 256 + ((n & 15) >> 2) * 64 + (kk >> 3) * 32 +
+                                (kk & 7) * 4 + (n & 3);
+                trdst[x] = (int)bcol_off(j) / 4 + e;
+                trq[x] = aq[src];
+                trk[x] = ak[src];
+            }
+        }
+
+        // this thread's column of its block, as (even row, odd row) pairs
+        float2 g2[BC / 2], k2[BC / 2];
+#pragma unroll
+        for (int m = 0; m < BC / 2; ++m) {
+            g2[m] = make_float2(sg[(r0 + 2 * m) * KD + d], sg[(r0 + 2 * m + 1) * KD + d]);
+            k2[m] = make_float2(to_f32(sk[(r0 + 2 * m) * KD + d]),
+                                to_f32(sk[(r0 + 2 * m + 1) * KD + d]));
+        }
+#define KDA_EL(arr, r) (((r) & 1) ? arr[(r) >> 1].y : arr[(r) >> 1].x)
+
+        // ---- prescaled TF32 operands and post-factors into TMEM ----
+        float c2 = 0.f, c3 = 0.f;  // 2^(g_16(i+2) - g_e(i)), 2^(g_16(i+3) - g_e(i))
+        if (i < NBLK - 1) {
+            const float ge = sg[(r0 + BC) * KD + d];
+            float a[BC], v[BC];
+#pragma unroll
+            for (int s = 0; s < BC; ++s) {
+                a[s] = ex2(ge - KDA_EL(g2, s));
+                v[s] = KDA_EL(k2, s) * a[s];
+            }
+            tc::tmem_st16(tlane + TM_FA + 16 * i, a);
+            tc::tmem_st16(tlane + tm_arow(i + 1) + 16 * i, v);
+            if (i + 2 < NBLK) {
+                c2 = ex2(sg[(r0 + 2 * BC) * KD + d] - ge);
+#pragma unroll
+                for (int s = 0; s < BC; ++s) a[s] = v[s] * c2;
+                tc::tmem_st16(tlane + tm_arow(i + 2) + 16 * i, a);
+            }
+            if (i + 3 < NBLK) {
+                c3 = ex2(sg[(r0 + 3 * BC) * KD + d] - ge);
+#pragma unroll
+                for (int s = 0; s < BC; ++s) a[s] = v[s] * c3;
+                tc::tmem_st16(tlane + tm_arow(i + 3) + 16 * i, a);
+            }
+        }
+        if (i > 0) {
+            float b[BC], v[BC];
+            b[0] = 1.f;
+#pragma unroll
+            for (int r = 1; r < BC; ++r) b[r] = ex2(KDA_EL(g2, r) - g2[0].x);
+            tc::tmem_st16(tlane + TM_FB + 16 * (i - 1), b);
+#pragma unroll
+            for (int r = 0; r < BC; ++r) v[r] = to_f32(sq[(r0 + r) * KD + d]) * b[r];
+            tc::tmem_st16(tlane + TM_AQB + 16 * (i - 1), v);
+#pragma unroll
+            for (int r = 0; r < BC; ++r) v[r] = sbeta[r0 + r] * KDA_EL(k2, r) * b[r];
+            tc::tmem_st16(tlane + TM_AKBB + 16 * (i - 1), v);
+        }
+
+        {
+            float *cq = reinterpret_cast<float *>(smem + SM_BCQ);
+            float *ck = reinterpret_cast<float *>(smem + SM_BCK);
+#pragma unroll
+            for (int x = 0; x < 3; ++x) {
+                cq[trdst[x]] = trq[x];
+                ck[trdst[x]] = trk[x];
+            }
+        }
+
+        // operands complete: TMEM stores landed, smem stores visible to the tensor core;
+        // the last warp to get here issues the 36 MMAs (no thread waits for the others)
+        tc::tmem_wait_st();
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncwarp();
+        uint32_t prev = 0;
+        if (lane == 0) prev = tc::atomic_add_acq_rel_smem(ops_count, 1u);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        // The branch is warp-uniform so the descriptor arithmetic stays on the uniform
+        // datapath; one elected lane issues.
+        if ((prev % TC_WARPS) == TC_WARPS - 1) {
+            tc::fence_after_sync();
+            const uint64_t dq0 = tc::smem_desc(tc::smem_u32(st + ST_DQ), 256, 128);
+            const uint64_t dk0 = tc::smem_desc(tc::smem_u32(st + ST_DK), 256, 128);
+            const uint64_t cq0 = tc::smem_desc(tc::smem_u32(smem + SM_BCQ), 128, 512);
+            const uint64_t ck0 = tc::smem_desc(tc::smem_u32(smem + SM_BCK), 128, 512);
+            const uint32_t id16 = tc::idesc_tf32(128, 16);
+            if (tc::elect_one()) {
+#pragma unroll
+                for (int t = 1; t < NBLK; ++t) {
+#pragma unroll
+                    for (int kk = 0; kk < 2 * t; ++kk) {
+                        const uint32_t a = tbase + tm_arow(t) + 8 * kk;
+                        const uint64_t boff = (uint64_t)((dablk(t, 0) * 1024 + 512 * kk) >> 4);
+                        tc::mma_tf32_ts(tbase + TM_XQ + 16 * (t - 1), a, dq0 + boff, id16, kk > 0);
+                        tc::mma_tf32_ts(tbase + TM_XK + 16 * (t - 1), a, dk0 + boff, id16, kk > 0);
+                    }
+                }
+#pragma unroll
+                for (int j = 1; j < NBLK; ++j) {
+                    const uint32_t idj = tc::idesc_tf32(128, 16 * j);
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk)
+                        tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AQB + 16 * (j - 1) + 8 * kk,
+                                        cq0 + ((bcol_off(j) + 256 * kk) >> 4), idj, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk)
+                        tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AKBB + 16 * (j - 1) + 8 * kk,
+                                        ck0 + ((bcol_off(j) + 256 * kk) >> 4), idj, true);
+                }
+                tc::mma_commit(mbar);
+            }
+        }
+        __syncwarp();
+
+        // ---- diagonal block: one exp2 per (r, s, d), shared by both sides, two source
+        // rows at a time in packed FP32x2.  Rows run in descending order: once row r is
+        // processed, its row sums and its column sum dkt[r] are complete, so each row is
+        // written out right away.  Rows 15..8 (92 of the 120 pairs) run before the MMA
+        // result is needed; rows 7..0 after it. ----
+        float accq[BC], acck[BC], dbv[BC];
+        float2 dkt2[BC / 2];
+#pragma unroll
+        for (int m = 0; m < BC / 2; ++m) dkt2[m] = make_float2(0.f, 0.f);
+        const float *dgq = reinterpret_cast<const float *>(st + ST_DQ) + dablk(i, i) * 256;
+        const float *dgk = reinterpret_cast<const float *>(st + ST_DK) + dablk(i, i) * 256;
+        const float2 neg1 = make_float2(-1.f, -1.f);
+        const Unit un = decode_unit(u, H, NT);
+        const size_t obase = grow(un, r0, T, H) * KD + d;
+        const uint32_t hk = (uint32_t)H * KD;
+
+        auto diag_row = [&](const int r) {
+            const float gv = KDA_EL(g2, r), kv = KDA_EL(k2, r);
+            const float qv = to_f32(sq[(r0 + r) * KD + d]);
+            const float kbr = sbeta[r0 + r] * kv;
+            const float2 grr = make_float2(gv, gv);
+            const float2 qq = make_float2(qv, qv);
+            const float2 kb2 = make_float2(kbr, kbr);
+            float2 aacc = make_float2(0.f, 0.f), kacc = make_float2(0.f, 0.f);
+            // row r's 16-byte chunk c of the diagonal block sits at c*64 + roff floats
+            const int roff = (r >> 3) * 32 + (r & 7) * 4;
+            // pairs (2m, 2m+1) cover s < r; for odd r the last pair is (r-1, r) and
+            // carries the diagonal term (E = 1, dAkk[r][r] outside the support -> 0)
+#pragma unroll
+            for (int c = 0; c < (r + 3) / 4; ++c) {
+                const float4 aq4 = *reinterpret_cast<const float4 *>(dgq + c * 64 + roff);
+                const float4 ak4 = *reinterpret_cast<const float4 *>(dgk + c * 64 + roff);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int m = 2 * c + h;
+                    if (2 * m < r) {
+                        const float2 aq = h ? make_float2(aq4.z, aq4.w) : make_float2(aq4.x, aq4.y);
+                        float2 ak = h ? make_float2(ak4.z, ak4.w) : make_float2(ak4.x, ak4.y);
+                        if (2 * m + 1 == r) ak.y = 0.f;
+                        const float2 df = __ffma2_rn(g2[m], neg1, grr);
+                        const float2 ev = make_float2(ex2(df.x), ex2(df.y));
+                        const float2 tq = __fmul2_rn(k2[m], ev);
+                        aacc = __ffma2_rn(aq, tq, aacc);
+                        kacc = __ffma2_rn(ak, tq, kacc);
+                        const float2 uu = __ffma2_rn(aq, qq, __fmul2_rn(ak, kb2));
+                        dkt2[m] = __ffma2_rn(uu, ev, dkt2[m]);
+                    }
+                }
+            }
+            accq[r] += aacc.x + aacc.y;
+            acck[r] += kacc.x + kacc.y;
+            if ((r & 1) == 0) {  // even r: the diagonal term on its own
+                const float aqd = dgq[(r >> 2) * 64 + roff + (r & 3)];
+                accq[r] = fmaf(aqd, kv, accq[r]);
+                dkt2[r >> 1].x = fmaf(aqd, qv, dkt2[r >> 1].x);
+            }
+        };
+        // incoming gradients (ACCUM): fetched three output rows ahead of their use
+        float inq[BC], ink[BC], ing[BC];
+        auto fetch_in = [&](const int r) {
+            if constexpr (ACCUM) {
+                const size_t off = obase + (size_t)((uint32_t)r * hk);
+                inq[r] = ex.dq_in ? __ldg(ex.dq_in + off) : 0.f;
+                ink[r] = ex.dk_in ? __ldg(ex.dk_in + off) : 0.f;
+                ing[r] = ex.dg_in ? __ldg(ex.dg_in + off) : 0.f;
+            }
+        };
+        float fold_run = 0.f;  // FOLD: running suffix sum of dg inside the sub-block
+        float *bank = reinterpret_cast<float *>(smem + SM_FOLD_BANK);
+        auto out_row = [&](const int r) {
+            const int row = r0 + r;
+            const size_t off = obase + (size_t)((uint32_t)r * hk);
+            if (r >= 3) fetch_in(r - 3);
+            const float qv = to_f32(sq[row * KD + d]);
+            const float kv = KDA_EL(k2, r), dkv = KDA_EL(dkt2, r);
+            const float pk = sbeta[row] * acck[r];
+            float vq = accq[r], vk = pk + dkv, vg = LN2 * fmaf(qv, accq[r], (pk - dkv) * kv);
+            if constexpr (ACCUM) {
+                vq += inq[r];
+                vk += ink[r];
+                vg += ing[r];
+            }
+            if constexpr (EMIT) {
+                reinterpret_cast<io_t *>(dq_out)[off] = from_f32<io_t>(vq);
+                reinterpret_cast<io_t *>(dk_out)[off] = from_f32<io_t>(vk);
+            } else {
+                dq[off] = vq;
+                dk[off] = vk;
+            }
+            if constexpr (FOLD) {
+                fold_run += vg;
+                bank[row * KD + d] = fold_run;
+            } else {
+                dg[off] = vg;
+            }
+            dbv[r] = acck[r] * kv;
+        };
+        // db[r] = sum over d of 8 rows at a time: transpose-reduce across the warp's lanes
+        // (lane l ends with row (l>>2)&7), then a fixed-order sum over the block's 4 warps.
+        auto db_rows = [&](const int rbase) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = dbv[rbase + j];
+#pragma unroll
+            for (int w = 4, m = 16; w >= 1; w >>= 1, m >>= 1) {
+                const bool hi = (lane & m) != 0;
+#pragma unroll
+                for (int j = 0; j < w; ++j) {
+                    const float send = hi ? v[j] : v[j + w];
+                    const float keep = hi ? v[j + w] : v[j];
+                    v[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                }
+            }
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+            if ((lane & 3) == 0) sdbp[(warp & 3) * BT + r0 + rbase + (lane >> 2)] = v[0];
+        };
+
+        fetch_in(BC - 1);
+        fetch_in(BC - 2);
+        fetch_in(BC - 3);
+#pragma unroll
+        for (int r = BC - 1; r >= BC / 2; --r) {
+            accq[r] = acck[r] = 0.f;
+            diag_row(r);
+        }
+
+        // ---- cross terms: wait for the MMAs, apply the post-factors ----
+        ok &= tc::mbar_wait(mbar, (uint32_t)it & 1u, SPIN_LIMIT);
+        tc::fence_after_sync();
+        if (i > 0) {
+            float f[BC], x[BC];
+            tc::tmem_ld16(tlane + TM_FB + 16 * (i - 1), f);
+            tc::tmem_ld16(tlane + TM_XQ + 16 * (i - 1), x);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int r = 0; r < BC; ++r) accq[r] = fmaf(f[r], x[r], r >= BC / 2 ? accq[r] : 0.f);
+            tc::tmem_ld16(tlane + TM_XK + 16 * (i - 1), x);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int r = 0; r < BC; ++r) acck[r] = fmaf(f[r], x[r], r >= BC / 2 ? acck[r] : 0.f);
+        } else {
+#pragma unroll
+            for (int r = 0; r < BC / 2; ++r) accq[r] = acck[r] = 0.f;
+        }
+        if (i < NBLK - 1) {
+            float y[BC], p[BC];
+            tc::tmem_ld16(tlane + tm_p(i + 1) + 16 * i, y);
+            tc::tmem_wait_ld();
+            if (i + 2 < NBLK) {
+                tc::tmem_ld16(tlane + tm_p(i + 2) + 16 * i, p);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int s = 0; s < BC; ++s) y[s] = fmaf(c2, p[s], y[s]);
+            }
+            if (i + 3 < NBLK) {
+                tc::tmem_ld16(tlane + tm_p(i + 3) + 16 * i, p);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int s = 0; s < BC; ++s) y[s] = fmaf(c3, p[s], y[s]);
+            }
+            tc::tmem_ld16(tlane + TM_FA + 16 * i, p);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int m = 0; m < BC / 2; ++m)
+                dkt2[m] = __ffma2_rn(make_float2(p[2 * m], p[2 * m + 1]),
+                                     make_float2(y[2 * m], y[2 * m + 1]), dkt2[m]);
+        }
+        if (!ok) {  // a wait gave up: poison this unit instead of hanging
+            const float nan = __int_as_float(0x7fc00000);
+#pragma unroll
+            for (int r = 0; r < BC; ++r) accq[r] = acck[r] = nan;
+#pragma unroll
+            for (int m = 0; m < BC / 2; ++m) dkt2[m] = make_float2(nan, nan);
+        }
+
+        // ---- rows 15..8 are complete: write them; then rows 7..0 ----
+#pragma unroll
+        for (int r = BC - 1; r >= BC / 2; --r) out_row(r);
+        db_rows(BC / 2);
+#pragma unroll
+        for (int r = BC / 2 - 1; r >= 0; --r) {
+            diag_row(r);
+            out_row(r);
+        }
+        db_rows(0);
+#undef KDA_EL
+        tc::named_bar_sync(1 + i, 128);
+        if ((warp & 3) == 0 && lane < BC) {
+            const int row = r0 + lane;
+            const size_t brow = grow(un, row, T, H);
+            float v = (sdbp[row] + sdbp[BT + row]) + (sdbp[2 * BT + row] + sdbp[3 * BT + row]);
+            if constexpr (ACCUM) {
+                if (ex.db_in) v += ex.db_in[brow];
+            }
+            db[brow] = v;
+        }
+        if constexpr (FOLD) {
+            // the four threads of channel d (one per sub-block, in warps c, c+4, c+8,
+            // c+12) exchange their sub-block totals; each adds the totals of the later
+            // sub-blocks to its banked in-block suffix sums
+            float *tot = reinterpret_cast<float *>(smem + SM_FOLD_TOT) + (it & 1) * NBLK * KD;
+            tot[i * KD + d] = fold_run;
+            tc::named_bar_sync(5 + (warp & 3), 128);
+            float later = 0.f;
+#pragma unroll
+            for (int j = NBLK - 1; j > 0; --j)
+                if (j > i) later += tot[j * KD + d];
+#pragma unroll
+            for (int r = 0; r < BC; ++r)
+                dg[obase + (size_t)((uint32_t)r * hk)] = bank[(r0 + r) * KD + d] + later;
+        }
+
+        // ---- unit done: the last warp releases the stage and refills it ----
+        tc::fence_before_sync();
+        __syncwarp();
+        prev = 0;
+        if (lane == 0) prev = tc::atomic_add_acq_rel_smem(done_count, 1u);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if ((prev % TC_WARPS) == TC_WARPS - 1 && u + 2 * stride < units) {
+            tc::fence_proxy_async_smem();
+            load_unit(st, &full[sidx], tm, beta, u + 2 * stride, T, H, ex.G, lane);
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tbase, TM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+// Defined once in kda_intra_tc.cu.
+cudaError_t make_maps(const BwdArgs &a, TmaMaps *tm);
+cudaError_t num_sms(int *n);
+
+template <typename io_t, bool ACCUM, bool FOLD, bool EMIT>
+cudaError_t launch_typed(const BwdArgs &a, cudaStream_t stream) {
+    auto kern = kda_intra_bwd_tc_kernel<io_t, ACCUM, FOLD, EMIT>;
+    const int smem_bytes = FOLD ? SM_TOTAL_FOLD : SM_TOTAL;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    int nsm = 0;
+    if ((e = num_sms(&nsm)) != cudaSuccess) return e;
+    TmaMaps tm;
+    if ((e = make_maps(a, &tm)) != cudaSuccess) return e;
+    const int HV = a.HV > 0 ? a.HV : a.H;
+    Extras ex;
+    ex.dq_in = a.dq_in;
+    ex.dk_in = a.dk_in;
+    ex.dg_in = a.dg_in;
+    ex.db_in = a.db_in;
+    ex.G = HV / a.H;
+    const long long units = (long long)a.B * HV * (a.T / BT);
+    const unsigned grid = (unsigned)(units < nsm ? units : nsm);
+    kern<<<grid, TC_THREADS, smem_bytes, stream>>>(tm, a.beta, a.dq, a.dk, a.db, a.dg, a.T, HV,
+                                                   units, ex);
+    return cudaGetLastError();
+}
+
+template <typename io_t, bool EMIT>
+cudaError_t launch_opts(const BwdArgs &a, cudaStream_t stream) {
+    const bool accum = a.dq_in || a.dk_in || a.dg_in || a.db_in;
+    if (accum)
+        return a.fold_dg ? launch_typed<io_t, true, true, EMIT>(a, stream)
+                         : launch_typed<io_t, true, false, EMIT>(a, stream);
+    return a.fold_dg ? launch_typed<io_t, false, true, EMIT>(a, stream)
+                     : launch_typed<io_t, false, false, EMIT>(a, stream);
+}
+
+template <typename io_t>
+cudaError_t launch_io(const BwdArgs &a, cudaStream_t stream) {
+    return a.emit_io ? launch_opts<io_t, true>(a, stream) : launch_opts<io_t, false>(a, stream);
+}
+
+}  // namespace tcimpl
+}  // namespace kda
