@@ -61,6 +61,36 @@ def algorithmic_bytes_per_unit(qk_bytes: int = 2, group: int = 1, accumulate: bo
     return qk + g + beta + da + out + acc
 
 
+def varlen_algorithmic_bytes(lens, H: int, qk_bytes: int = 2, accumulate: bool = False,
+                             io_out: bool = False) -> float:
+    """algorithmic_bytes_per_unit summed over the chunks of variable-length sequences
+    (chunks restart at each sequence start; a short chunk moves its valid rows and the
+    lower-block part of their dA rows only), times H heads."""
+    bt, kd, bc = kda_inputs.BT, kda_inputs.K, 16
+    per_row = (2 * kd * qk_bytes + kd * 4 + 4                # q, k, g, beta
+               + 2 * kd * (qk_bytes if io_out else 4) + kd * 4 + 4  # dq, dk, dg, db
+               + (3 * kd * 4 + 4 if accumulate else 0))
+    total = 0
+    for n in lens:
+        for c0 in range(0, n, bt):
+            m = min(bt, n - c0)
+            total += m * per_row + 2 * 4 * sum(bc * (r // bc + 1) for r in range(m))
+    return float(total * H)
+
+
+class VarlenWorkload:
+    """The variable-length workload, with the attributes of a kda_inputs.Config."""
+
+    def __init__(self, cu):
+        w = kda_inputs.VARLEN_WORKLOAD
+        self.lens = (cu[1:] - cu[:-1]).tolist()
+        self.name, self.B, self.T, self.H = w["name"], 1, int(cu[-1]), w["H"]
+        self.gate_lo, self.qk_dtype = w["gate_lo"], torch.bfloat16
+        self.chunks = sum(-(-n // kda_inputs.BT) for n in self.lens)
+        self.units = self.chunks * self.H
+        self.tokens_heads = self.T * self.H
+
+
 KERNEL_SOURCES = {
     "kda_intra_bwd_tc_kernel": ("kda_intra_tc.cuh", "kda_intra_tc.cu", "tc_ptx.cuh", "kda_common.cuh"),
     "kda_intra_bwd_fp32_kernel": ("kda_intra_fp32.cu", "kda_common.cuh"),
@@ -213,6 +243,13 @@ def config_dict(cfg, path, opts=None):
     }
     if opts:
         d["options"] = opts
+    if isinstance(cfg, VarlenWorkload):
+        d["sequences"] = {"count": len(cfg.lens), "min": min(cfg.lens), "max": max(cfg.lens),
+                          "not_whole_chunks": sum(1 for n in cfg.lens if n % kda_inputs.BT),
+                          "chunks": cfg.chunks,
+                          "recipe": "log-uniform lengths in [1, 8192], seeded"}
+        d["l2"] = "no flush: inputs+outputs of one step (%.2f GB) exceed the 129 MB L2" % (
+            varlen_algorithmic_bytes(cfg.lens, cfg.H) / 1e9)
     return d
 
 
@@ -311,27 +348,36 @@ def run_ours(args, cfg):
     kda.load_library()
     stream = torch.cuda.current_stream(dev)
     seed = kda_inputs.SEED0 + args.config + 1000 * rank
-    cpu = kda_inputs.make_inputs(cfg.B, cfg.T, cfg.H, gate_lo=cfg.gate_lo,
-                                 qk_dtype=cfg.qk_dtype, seed=seed)
+    if args.varlen:
+        cpu, cu = kda_inputs.make_varlen_workload(kda_inputs.SEED0 + 1000 * rank)
+        cfg = VarlenWorkload(cu)
+        varlen = {"cu_seqlens": cu.to(dev),
+                  "chunk_indices": kda.prepare_chunk_indices(cu).to(dev)}
+    else:
+        cpu = kda_inputs.make_inputs(cfg.B, cfg.T, cfg.H, gate_lo=cfg.gate_lo,
+                                     qk_dtype=cfg.qk_dtype, seed=seed)
+        varlen = {}
     if args.gva > 1:  # q/k shared by groups of value heads
         cpu["q"] = cpu["q"][:, :, ::args.gva].contiguous()
         cpu["k"] = cpu["k"][:, :, ::args.gva].contiguous()
     x = {n: v.to(dev) for n, v in cpu.items()}
     ins = [x[n] for n in ("q", "k", "g", "beta", "dAqk", "dAkk")]
-    extended = args.gva > 1 or args.accumulate or args.fold_dg or args.io_dtype_out
+    extended = (args.gva > 1 or args.accumulate or args.fold_dg or args.io_dtype_out
+                or args.varlen)
     opts = None
     if extended:
         gen = torch.Generator().manual_seed(seed + 1)
-        extra = {}
+        extra = dict(varlen)
         if args.accumulate:
             shp = (cfg.B, cfg.T, cfg.H, kda_inputs.K)
-            extra = {n: torch.randn(*shp, generator=gen).to(dev)
-                     for n in ("dq_in", "dk_in", "dg_in")}
+            extra.update({n: torch.randn(*shp, generator=gen).to(dev)
+                          for n in ("dq_in", "dk_in", "dg_in")})
             extra["db_in"] = torch.randn(cfg.B, cfg.T, cfg.H, generator=gen).to(dev)
         outs = list(kda.kda_intra_bwd_ex(*ins, **extra, fold_dg=args.fold_dg,
                                          dqdk_io_dtype=args.io_dtype_out))
         opts = {"value_heads_per_qk_head": args.gva, "accumulate": args.accumulate,
-                "fold_dg": args.fold_dg, "dqdk_io_dtype": args.io_dtype_out}
+                "fold_dg": args.fold_dg, "dqdk_io_dtype": args.io_dtype_out,
+                "varlen": args.varlen}
 
         def step():
             kda.kda_intra_bwd_ex(*ins, *outs, **extra, fold_dg=args.fold_dg,
@@ -404,9 +450,16 @@ def run_ours(args, cfg):
 
     if rank != 0:
         return
-    bytes_per_launch = cfg.units * algorithmic_bytes_per_unit(
-        torch.tensor([], dtype=cfg.qk_dtype).element_size(), group=args.gva,
-        accumulate=args.accumulate, io_out=args.io_dtype_out)
+    qk_bytes = torch.tensor([], dtype=cfg.qk_dtype).element_size()
+    if args.varlen:
+        bytes_per_launch = varlen_algorithmic_bytes(cfg.lens, cfg.H, qk_bytes,
+                                                    accumulate=args.accumulate,
+                                                    io_out=args.io_dtype_out)
+        if args.gva > 1:
+            bytes_per_launch -= cfg.T * cfg.H * 2 * kda_inputs.K * qk_bytes * (1 - 1 / args.gva)
+    else:
+        bytes_per_launch = cfg.units * algorithmic_bytes_per_unit(
+            qk_bytes, group=args.gva, accumulate=args.accumulate, io_out=args.io_dtype_out)
     achieved = bytes_per_launch / (ms / args.steps / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
     kname = KERNEL_NAMES[args.path]
@@ -453,6 +506,9 @@ def main():
                    help="dg as its chunk-local reverse cumsum (kda_intra_bwd_ex)")
     p.add_argument("--io-dtype-out", action="store_true",
                    help="dq, dk written in the q/k dtype (kda_intra_bwd_ex)")
+    p.add_argument("--varlen", action="store_true",
+                   help="the variable-length workload (32768 tokens x 16 heads in "
+                        "sequences of log-uniform length) through cu_seqlens")
     args = p.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     cfg = kda_inputs.CONFIGS[args.config]

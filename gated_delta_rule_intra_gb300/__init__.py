@@ -10,7 +10,8 @@ The functions carry the C names of ``include/kda.h``:
 * ``kda_intra_bwd_fp32``  -- all-FP32 path
 * ``kda_intra_bwd_ex``    -- fast path with options: grouped value heads, incoming
   gradients added in-kernel, dg folded to its chunk-local reverse cumsum, dq/dk in
-  the q/k dtype
+  the q/k dtype, variable-length sequences (``cu_seqlens``)
+* ``prepare_chunk_indices`` -- the (sequence, chunk) table of a ``cu_seqlens``
 * ``kda_intra_bwd_host``  -- host buffers in and out, copies on the stream
 * ``kda_status_str``, ``kda_abi_version``
 """
@@ -39,7 +40,9 @@ class KdaOpts(ctypes.Structure):
     """Mirror of kda_intra_bwd_opts_t."""
     _fields_ = [("HV", ctypes.c_int), ("dq_in", ctypes.c_void_p), ("dk_in", ctypes.c_void_p),
                 ("dg_in", ctypes.c_void_p), ("db_in", ctypes.c_void_p),
-                ("fold_dg", ctypes.c_int), ("dqdk_io_dtype", ctypes.c_int)]
+                ("fold_dg", ctypes.c_int), ("dqdk_io_dtype", ctypes.c_int),
+                ("cu_seqlens", ctypes.c_void_p), ("chunk_indices", ctypes.c_void_p),
+                ("num_seqs", ctypes.c_int), ("num_chunks", ctypes.c_int)]
 
 
 class KdaError(RuntimeError):
@@ -174,9 +177,30 @@ def kda_intra_bwd_fp32(q, k, g, beta, dAqk, dAkk, dq=None, dk=None, db=None, dg=
                         stream)
 
 
+def prepare_chunk_indices(cu_seqlens, bt: int = BT):
+    """The chunk table of packed variable-length sequences: an int32 [num_chunks, 2]
+    tensor on cu_seqlens' device whose row c is (n, j) = chunk j of sequence n, in
+    sequence order (sequence n covers tokens [cu_seqlens[n], cu_seqlens[n+1]) and has
+    ceil(len / bt) chunks; empty sequences have none).  Reads cu_seqlens on the host."""
+    cu = torch.as_tensor(cu_seqlens).to("cpu", torch.int64)
+    if cu.dim() != 1 or cu.numel() < 2:
+        raise ValueError("cu_seqlens must be 1-d with at least two entries")
+    lens = cu[1:] - cu[:-1]
+    if cu[0].item() != 0 or bool((lens < 0).any()):
+        raise ValueError("cu_seqlens must start at 0 and be non-decreasing")
+    nch = (lens + bt - 1) // bt
+    seq = torch.repeat_interleave(torch.arange(len(nch)), nch)
+    first = torch.cumsum(nch, 0) - nch
+    idx = torch.arange(int(nch.sum())) - torch.repeat_interleave(first, nch)
+    out = torch.stack([seq, idx], dim=1).to(torch.int32)
+    dev = cu_seqlens.device if isinstance(cu_seqlens, torch.Tensor) else "cpu"
+    return out.to(dev).contiguous()
+
+
 def kda_intra_bwd_ex(q, k, g, beta, dAqk, dAkk, dq=None, dk=None, db=None, dg=None, *,
                      dq_in=None, dk_in=None, dg_in=None, db_in=None, fold_dg=False,
-                     dqdk_io_dtype=False, stream=None):
+                     dqdk_io_dtype=False, cu_seqlens=None, chunk_indices=None,
+                     stream=None):
     """Intra-chunk backward with the extended options of ``kda_intra_bwd_ex``.
 
     q, k have H heads; g, beta, dAqk, dAkk, the outputs and the optional incoming
@@ -184,6 +208,9 @@ def kda_intra_bwd_ex(q, k, g, beta, dAqk, dAkk, dq=None, dk=None, db=None, dg=No
     ``dq_in``.. ``db_in`` are added in-kernel (they may be the output tensors
     themselves); ``fold_dg`` returns dg as its inclusive reverse cumsum inside each
     64-token chunk; ``dqdk_io_dtype`` writes dq and dk in q's dtype.
+    ``cu_seqlens`` (int32 [N + 1] on the device, B must be 1) packs N sequences of any
+    length along T; ``chunk_indices`` (int32 [num_chunks, 2] on the device) defaults to
+    ``prepare_chunk_indices(cu_seqlens)``, which reads cu_seqlens on the host.
     Returns (dq, dk, db, dg).
     """
     if q.device.type != "cuda":
@@ -219,6 +246,17 @@ def kda_intra_bwd_ex(q, k, g, beta, dAqk, dAkk, dq=None, dk=None, db=None, dg=No
             setattr(opts, name, t.data_ptr())
     opts.fold_dg = int(bool(fold_dg))
     opts.dqdk_io_dtype = int(bool(dqdk_io_dtype))
+    if cu_seqlens is not None:
+        if chunk_indices is None:
+            chunk_indices = prepare_chunk_indices(cu_seqlens)
+        _check("cu_seqlens", cu_seqlens, (cu_seqlens.numel(),), torch.int32, dev)
+        _check("chunk_indices", chunk_indices, (chunk_indices.shape[0], 2), torch.int32, dev)
+        opts.cu_seqlens = cu_seqlens.data_ptr()
+        opts.chunk_indices = chunk_indices.data_ptr() if chunk_indices.numel() else 0
+        opts.num_seqs = cu_seqlens.numel() - 1
+        opts.num_chunks = chunk_indices.shape[0]
+    elif chunk_indices is not None:
+        raise ValueError("chunk_indices needs cu_seqlens")
     lib = load_library()
     ptr = ctypes.c_void_p
     with torch.cuda.device(dev):

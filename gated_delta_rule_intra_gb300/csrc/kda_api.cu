@@ -20,9 +20,9 @@ struct Range {
 
 bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
-kda_status_t check_shape(int B, int T, int H) {
+kda_status_t check_shape(int B, int T, int H, bool varlen = false) {
     if (B <= 0 || T <= 0 || H <= 0 || H > KDA_MAX_H) return KDA_ERR_SHAPE;
-    if (T % KDA_BT != 0) return KDA_ERR_SHAPE;
+    if (!varlen && T % KDA_BT != 0) return KDA_ERR_SHAPE;
     const long long rows = (long long)B * T * H;
     const long long units = rows / KDA_BT;
     if (units > 0x7fffffffLL) return KDA_ERR_SHAPE;     // grid limit
@@ -93,7 +93,15 @@ kda_status_t check_ex(const void *q, const void *k, const float *g, const float 
         return KDA_ERR_NULL;
     const int HV = o.HV ? o.HV : H;
     if (H <= 0 || HV <= 0 || HV % H != 0) return KDA_ERR_SHAPE;
-    kda_status_t st = check_shape(B, T, HV);
+    const bool varlen = o.cu_seqlens || o.chunk_indices;
+    if (varlen) {
+        if (!o.cu_seqlens || (!o.chunk_indices && o.num_chunks > 0)) return KDA_ERR_NULL;
+        if (B != 1 || o.num_seqs <= 0 || o.num_chunks < 0) return KDA_ERR_SHAPE;
+        if ((long long)o.num_chunks * HV > 0x7fffffffLL) return KDA_ERR_SHAPE;
+        if ((uintptr_t)o.cu_seqlens % 4u || (uintptr_t)o.chunk_indices % 4u)
+            return KDA_ERR_ALIGN;
+    }
+    kda_status_t st = check_shape(B, T, HV, varlen);
     if (st != KDA_OK) return st;
     if (dt != KDA_BF16 && dt != KDA_FP16) return KDA_ERR_DTYPE;
     if (o.fold_dg != 0 && o.fold_dg != 1) return KDA_ERR_OPTION;
@@ -114,6 +122,10 @@ kda_status_t check_ex(const void *q, const void *k, const float *g, const float 
         {(uintptr_t)beta, (uintptr_t)beta + rv * 4},
         {(uintptr_t)dAqk, (uintptr_t)dAqk + rv * KDA_BT * 4},
         {(uintptr_t)dAkk, (uintptr_t)dAkk + rv * KDA_BT * 4},
+        {(uintptr_t)o.cu_seqlens,
+         varlen ? (uintptr_t)o.cu_seqlens + ((size_t)o.num_seqs + 1) * 4 : 0},
+        {(uintptr_t)o.chunk_indices,
+         varlen ? (uintptr_t)o.chunk_indices + (size_t)o.num_chunks * 8 : 0},
     };
     const Range opt_in[] = {
         {(uintptr_t)o.dq_in, o.dq_in ? (uintptr_t)o.dq_in + rv * KDA_K * 4 : 0},
@@ -194,6 +206,10 @@ kda_status_t kda_intra_bwd_ex(const void *q, const void *k, const float *g,
     a.db_in = o.db_in;
     a.fold_dg = o.fold_dg != 0;
     a.emit_io = o.dqdk_io_dtype != 0;
+    a.cu_seqlens = o.cu_seqlens;
+    a.chunk_indices = o.chunk_indices;
+    a.num_seqs = o.num_seqs;
+    a.num_chunks = o.num_chunks;
     return kda::launch_intra_tc(a, (cudaStream_t)stream) == cudaSuccess ? KDA_OK
                                                                         : KDA_ERR_CUDA;
 }
@@ -277,7 +293,8 @@ const char *kda_status_str(kda_status_t status) {
         case KDA_OK: return "KDA_OK";
         case KDA_ERR_NULL: return "KDA_ERR_NULL: a required pointer is NULL";
         case KDA_ERR_SHAPE:
-            return "KDA_ERR_SHAPE: need B,T > 0, 0 < H <= 65536 and T % 64 == 0";
+            return "KDA_ERR_SHAPE: need B,T > 0, 0 < H <= 65536 and T % 64 == 0 "
+                   "(varlen: B == 1, num_seqs > 0, num_chunks >= 0)";
         case KDA_ERR_DTYPE: return "KDA_ERR_DTYPE: qk_dtype must be KDA_BF16 or KDA_FP16";
         case KDA_ERR_ALIGN: return "KDA_ERR_ALIGN: a pointer is misaligned";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA call or kernel launch failed";

@@ -1,11 +1,14 @@
 // Host side of the tensor-core kernel: tensor maps, the SM count, and the dispatch
-// to the per-element-type instantiations (kda_intra_tc_bf16.cu, kda_intra_tc_fp16.cu).
+// to the instantiations per q/k element type and sequence layout
+// (kda_intra_tc_{bf16,fp16}[_varlen].cu).
 #include "kda_intra_tc.cuh"
 
 namespace kda {
 
 cudaError_t launch_tc_bf16(const BwdArgs &a, cudaStream_t stream);
 cudaError_t launch_tc_fp16(const BwdArgs &a, cudaStream_t stream);
+cudaError_t launch_tc_bf16_varlen(const BwdArgs &a, cudaStream_t stream);
+cudaError_t launch_tc_fp16_varlen(const BwdArgs &a, cudaStream_t stream);
 
 namespace tcimpl {
 namespace {
@@ -58,17 +61,31 @@ cudaError_t make_maps(const BwdArgs &a, TmaMaps *tm) {
             cudaSuccess)
             return e;
     }
-    {  // dA: (col%4, row%8, row/8, col/4, head); one box = one 16x16 block laid out as a
-       // tensor-core operand (4 floats, 8 rows, 2 row groups, 4 column chunks)
+    // no L2 promotion for dA: a promoted fetch would also pull the rows' unused upper part
+    const CUtensorMapL2promotion l2 = CU_TENSOR_MAP_L2_PROMOTION_NONE;
+    if (!a.cu_seqlens) {
+        // dA: (col%4, row%8, row/8, col/4, head); one box = one 16x16 block laid out as a
+        // tensor-core operand (4 floats, 8 rows, 2 row groups, 4 column chunks)
         const cuuint64_t dims[5] = {4, 8, rows / 8, BT / 4, H};
         const cuuint64_t str[4] = {H * BT * 4, 8 * H * BT * 4, 16, BT * 4};
         const cuuint32_t box[5] = {4, 8, 2, 4, 1};
-        // no L2 promotion: a promoted fetch would also pull the rows' unused upper part
-        const CUtensorMapL2promotion l2 = CU_TENSOR_MAP_L2_PROMOTION_NONE;
         if ((e = encode(&tm->daqk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, a.dAqk, dims, str, box,
                         l2)) != cudaSuccess)
             return e;
         if ((e = encode(&tm->dakk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, a.dAkk, dims, str, box,
+                        l2)) != cudaSuccess)
+            return e;
+    } else {
+        // variable-length units start at any row: (col%4, row, col/4, head), box
+        // (4, 16, 4, 1) -- the same bytes in the same operand layout (row n of the block
+        // at n*16 bytes inside each 256-byte column chunk)
+        const cuuint64_t dims[4] = {4, rows, BT / 4, H};
+        const cuuint64_t str[3] = {H * BT * 4, 16, BT * 4};
+        const cuuint32_t box[4] = {4, BC, 4, 1};
+        if ((e = encode(&tm->daqk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.dAqk, dims, str, box,
+                        l2)) != cudaSuccess)
+            return e;
+        if ((e = encode(&tm->dakk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.dAkk, dims, str, box,
                         l2)) != cudaSuccess)
             return e;
     }
@@ -92,6 +109,8 @@ cudaError_t num_sms(int *n) {
 }  // namespace tcimpl
 
 cudaError_t launch_intra_tc(const BwdArgs &a, cudaStream_t stream) {
+    if (a.cu_seqlens)
+        return a.fp16 ? launch_tc_fp16_varlen(a, stream) : launch_tc_bf16_varlen(a, stream);
     return a.fp16 ? launch_tc_fp16(a, stream) : launch_tc_bf16(a, stream);
 }
 

@@ -68,7 +68,8 @@ constexpr int SM_FULL = SM_DBP + 1024;       // 2 stage-full mbarriers
 constexpr int SM_MMA = SM_FULL + 16;         // MMAs-done mbarrier
 constexpr int SM_CNT = SM_MMA + 8;           // operand counter, unit-done counter
 constexpr int SM_TSLOT = SM_CNT + 8;
-constexpr int SM_TOTAL = SM_TSLOT + 8;
+constexpr int SM_META = SM_TSLOT + 8;        // varlen: per stage {first token row, valid rows}
+constexpr int SM_TOTAL = SM_META + 16;
 // extra shared memory of the fold_dg variant: the per-row dg bank [64][128] and the
 // per-(sub-block, channel) totals, double-buffered by unit parity
 constexpr int SM_FOLD_BANK = (SM_TOTAL + 127) / 128 * 128;
@@ -107,7 +108,38 @@ struct TmaMaps {
 struct Extras {
     const float *dq_in, *dk_in, *dg_in, *db_in;  // added in-kernel when non-null
     int G;  // value heads per q/k head
+    // variable-length launches: sequence n is tokens [cu_seqlens[n], cu_seqlens[n+1])
+    // of the packed T axis; unit u is head u % H of chunk chunk_indices[2c+1] of
+    // sequence chunk_indices[2c], c = u / H
+    const int *cu_seqlens, *chunk_indices;
+    int num_seqs;
 };
+
+// Where a variable-length unit lives: first token row, valid rows (1..64; 0 for an
+// entry of chunk_indices that names no chunk of cu_seqlens, which is then skipped)
+// and head.
+struct VarUnit {
+    int start, len, h;
+};
+
+__device__ __forceinline__ VarUnit varlen_unit(long long u, int H, int T, const Extras ex) {
+    const unsigned uu = (unsigned)u, c = uu / (unsigned)H;
+    VarUnit x;
+    x.h = (int)(uu - c * (unsigned)H);
+    x.start = 0;
+    x.len = 0;
+    const int n = __ldg(ex.chunk_indices + 2 * (size_t)c);
+    const int ci = __ldg(ex.chunk_indices + 2 * (size_t)c + 1);
+    if (n >= 0 && n < ex.num_seqs && ci >= 0) {
+        const long long bos = __ldg(ex.cu_seqlens + n), eos = __ldg(ex.cu_seqlens + n + 1);
+        const long long st = bos + (long long)BT * ci;
+        if (bos >= 0 && st < eos && eos <= T) {
+            x.start = (int)st;
+            x.len = (int)(eos - st < BT ? eos - st : BT);
+        }
+    }
+    return x;
+}
 
 template <typename T> __device__ __forceinline__ T from_f32(float x);
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
@@ -121,44 +153,85 @@ __device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
     uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(gmem) : "memory");
 }
+// Same, or four zero bytes (nothing read) when !take.
+__device__ __forceinline__ void cp_async4_zfill(void *smem, const void *gmem, bool take) {
+    uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(s), "l"(gmem),
+                 "r"(take ? 4 : 0)
+                 : "memory");
+}
 
 // One warp queues every copy of one unit into a stage: 23 TMA tiles from lane 0,
 // beta as 64 four-byte copies from all lanes (its rows are H floats apart, so no
-// tensor map can describe it when H is not a multiple of 4).
-__device__ __forceinline__ void load_unit(unsigned char *st, uint64_t *full,
+// tensor map can describe it when H is not a multiple of 4).  A variable-length unit
+// may start at any token row: its dA tiles come through the 4-d map (any row start),
+// rows past the sequence's end are loaded as they are (or zero-filled past the
+// tensor's end) and masked by the consumer, and their beta is zero-filled.  Lane 0
+// records the unit's row range in `meta` before its arrival on the stage barrier,
+// which publishes it with the data.
+template <bool VARLEN>
+__device__ __forceinline__ void load_unit(unsigned char *st, uint64_t *full, int *meta,
                                           const TmaMaps &tm, const float *__restrict__ beta,
-                                          long long u, int T, int H, int G, int lane) {
-    const Unit x = decode_unit(u, H, T / BT);
-    const int row = x.b * T + x.c * BT;  // first token row of the unit
+                                          long long u, int T, int H, const Extras ex,
+                                          int lane) {
+    int row, h, len = BT;  // first token row of the unit, head, valid rows
+    if constexpr (VARLEN) {
+        const VarUnit x = varlen_unit(u, H, T, ex);
+        row = x.start;
+        len = x.len;
+        h = x.h;
+        if (lane == 0) {
+            meta[0] = row;
+            meta[1] = len;
+        }
+    } else {
+        const Unit x = decode_unit(u, H, T / BT);
+        row = x.b * T + x.c * BT;
+        h = x.h;
+    }
     if (lane == 0) {
         tc::mbar_arrive_expect_tx(full, STAGE_TX_BYTES);
-        tc::tma_load_3d(st + ST_Q, &tm.q, 0, x.h / G, row, full);
-        tc::tma_load_3d(st + ST_K, &tm.k, 0, x.h / G, row, full);
-        tc::tma_load_3d(st + ST_G, &tm.g, 0, x.h, row, full);
+        tc::tma_load_3d(st + ST_Q, &tm.q, 0, h / ex.G, row, full);
+        tc::tma_load_3d(st + ST_K, &tm.k, 0, h / ex.G, row, full);
+        tc::tma_load_3d(st + ST_G, &tm.g, 0, h, row, full);
 #pragma unroll
         for (int t = 0; t < NBLK; ++t) {
 #pragma unroll
             for (int j = 0; j <= t; ++j) {
-                const int rg = (row + BC * t) >> 3;
-                tc::tma_load_5d(st + ST_DQ + dablk(t, j) * 1024, &tm.daqk, 0, 0, rg, 4 * j, x.h,
-                                full);
-                tc::tma_load_5d(st + ST_DK + dablk(t, j) * 1024, &tm.dakk, 0, 0, rg, 4 * j, x.h,
-                                full);
+                if constexpr (VARLEN) {
+                    tc::tma_load_4d(st + ST_DQ + dablk(t, j) * 1024, &tm.daqk, 0, row + BC * t,
+                                    4 * j, h, full);
+                    tc::tma_load_4d(st + ST_DK + dablk(t, j) * 1024, &tm.dakk, 0, row + BC * t,
+                                    4 * j, h, full);
+                } else {
+                    const int rg = (row + BC * t) >> 3;
+                    tc::tma_load_5d(st + ST_DQ + dablk(t, j) * 1024, &tm.daqk, 0, 0, rg, 4 * j,
+                                    h, full);
+                    tc::tma_load_5d(st + ST_DK + dablk(t, j) * 1024, &tm.dakk, 0, 0, rg, 4 * j,
+                                    h, full);
+                }
             }
         }
     }
-    const size_t b0 = grow(x, 0, T, H);
+    const float *b0 = beta + (size_t)row * H + h;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
         const int r = lane + 32 * e;
-        cp_async4(st + ST_BETA + r * 4, beta + b0 + (size_t)r * H);
+        if constexpr (VARLEN)
+            cp_async4_zfill(st + ST_BETA + r * 4, r < len ? b0 + (size_t)r * H : beta, r < len);
+        else
+            cp_async4(st + ST_BETA + r * 4, b0 + (size_t)r * H);
     }
     tc::cp_async_mbar_arrive_noinc(full);
 }
 
 // ACCUM: add the optional incoming gradients of Extras; FOLD: return dg as its
-// inclusive reverse cumsum inside each chunk; EMIT: store dq and dk as io_t.
-template <typename io_t, bool ACCUM, bool FOLD, bool EMIT>
+// inclusive reverse cumsum inside each chunk; EMIT: store dq and dk as io_t;
+// VARLEN: units come from cu_seqlens / chunk_indices, and a unit's rows past its
+// sequence's end (row >= len) are masked: their q, k and beta read as 0, their gate
+// as the last valid row's (so every exponent stays <= 0), their dA rows take no part
+// in the column-side sums, and nothing is written for them.
+template <typename io_t, bool ACCUM, bool FOLD, bool EMIT, bool VARLEN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restrict__ beta,
                         void *dq_out, void *dk_out, float *db, float *dg, int T, int H,
@@ -199,11 +272,13 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
     const uint32_t tbase = *tslot;
     const uint32_t tlane = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
 
+    int *meta = reinterpret_cast<int *>(smem + SM_META);
     if (warp == 0) {  // the first two units of this CTA
         const long long u0 = blockIdx.x;
-        if (u0 < units) load_unit(smem, &full[0], tm, beta, u0, T, H, ex.G, lane);
+        if (u0 < units) load_unit<VARLEN>(smem, &full[0], meta, tm, beta, u0, T, H, ex, lane);
         if (u0 + stride < units)
-            load_unit(smem + STAGE_BYTES, &full[1], tm, beta, u0 + stride, T, H, ex.G, lane);
+            load_unit<VARLEN>(smem + STAGE_BYTES, &full[1], meta + 2, tm, beta, u0 + stride, T,
+                              H, ex, lane);
     }
 
     bool ok = true;
@@ -217,6 +292,11 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         const io_t *sq = reinterpret_cast<const io_t *>(st + ST_Q);
         const io_t *sk = reinterpret_cast<const io_t *>(st + ST_K);
         const float *sbeta = reinterpret_cast<const float *>(st + ST_BETA);
+        // valid rows of this unit and the last of them (rows past it take its gate)
+        int ulen = BT;
+        if constexpr (VARLEN) ulen = meta[2 * sidx + 1];
+        const int glast = ulen > 0 ? ulen - 1 : 0;
+        auto grow_g = [&](const int r) { return VARLEN ? min(r, glast) : r; };
 
         // ---- column-side B operands: dA blocks (j, 0..j-1) transposed.  The loads go
         // out first so their latency overlaps the column loads and the prescale. ----
@@ -238,6 +318,7 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
                 trdst[x] = (int)bcol_off(j) / 4 + e;
                 trq[x] = aq[src];
                 trk[x] = ak[src];
+                if (VARLEN && BC * j + kk >= ulen) trq[x] = trk[x] = 0.f;
             }
         }
 
@@ -245,16 +326,18 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         float2 g2[BC / 2], k2[BC / 2];
 #pragma unroll
         for (int m = 0; m < BC / 2; ++m) {
-            g2[m] = make_float2(sg[(r0 + 2 * m) * KD + d], sg[(r0 + 2 * m + 1) * KD + d]);
-            k2[m] = make_float2(to_f32(sk[(r0 + 2 * m) * KD + d]),
-                                to_f32(sk[(r0 + 2 * m + 1) * KD + d]));
+            const int ra = r0 + 2 * m, rb = ra + 1;
+            g2[m] = make_float2(sg[grow_g(ra) * KD + d], sg[grow_g(rb) * KD + d]);
+            k2[m] = make_float2(to_f32(sk[ra * KD + d]), to_f32(sk[rb * KD + d]));
+            if (VARLEN && ra >= ulen) k2[m].x = 0.f;
+            if (VARLEN && rb >= ulen) k2[m].y = 0.f;
         }
 #define KDA_EL(arr, r) (((r) & 1) ? arr[(r) >> 1].y : arr[(r) >> 1].x)
 
         // ---- prescaled TF32 operands and post-factors into TMEM ----
         float c2 = 0.f, c3 = 0.f;  // 2^(g_16(i+2) - g_e(i)), 2^(g_16(i+3) - g_e(i))
         if (i < NBLK - 1) {
-            const float ge = sg[(r0 + BC) * KD + d];
+            const float ge = sg[grow_g(r0 + BC) * KD + d];
             float a[BC], v[BC];
 #pragma unroll
             for (int s = 0; s < BC; ++s) {
@@ -264,13 +347,13 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             tc::tmem_st16(tlane + TM_FA + 16 * i, a);
             tc::tmem_st16(tlane + tm_arow(i + 1) + 16 * i, v);
             if (i + 2 < NBLK) {
-                c2 = ex2(sg[(r0 + 2 * BC) * KD + d] - ge);
+                c2 = ex2(sg[grow_g(r0 + 2 * BC) * KD + d] - ge);
 #pragma unroll
                 for (int s = 0; s < BC; ++s) a[s] = v[s] * c2;
                 tc::tmem_st16(tlane + tm_arow(i + 2) + 16 * i, a);
             }
             if (i + 3 < NBLK) {
-                c3 = ex2(sg[(r0 + 3 * BC) * KD + d] - ge);
+                c3 = ex2(sg[grow_g(r0 + 3 * BC) * KD + d] - ge);
 #pragma unroll
                 for (int s = 0; s < BC; ++s) a[s] = v[s] * c3;
                 tc::tmem_st16(tlane + tm_arow(i + 3) + 16 * i, a);
@@ -283,7 +366,8 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             for (int r = 1; r < BC; ++r) b[r] = ex2(KDA_EL(g2, r) - g2[0].x);
             tc::tmem_st16(tlane + TM_FB + 16 * (i - 1), b);
 #pragma unroll
-            for (int r = 0; r < BC; ++r) v[r] = to_f32(sq[(r0 + r) * KD + d]) * b[r];
+            for (int r = 0; r < BC; ++r)
+                v[r] = (VARLEN && r0 + r >= ulen) ? 0.f : to_f32(sq[(r0 + r) * KD + d]) * b[r];
             tc::tmem_st16(tlane + TM_AQB + 16 * (i - 1), v);
 #pragma unroll
             for (int r = 0; r < BC; ++r) v[r] = sbeta[r0 + r] * KDA_EL(k2, r) * b[r];
@@ -358,8 +442,15 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         const float *dgq = reinterpret_cast<const float *>(st + ST_DQ) + dablk(i, i) * 256;
         const float *dgk = reinterpret_cast<const float *>(st + ST_DK) + dablk(i, i) * 256;
         const float2 neg1 = make_float2(-1.f, -1.f);
-        const Unit un = decode_unit(u, H, NT);
-        const size_t obase = grow(un, r0, T, H) * KD + d;
+        size_t orow0;  // output row (token * H + head) of row r0
+        if constexpr (VARLEN) {
+            orow0 = (size_t)(meta[2 * sidx] + r0) * H + (int)((unsigned)u % (unsigned)H);
+        } else {
+            const Unit un = decode_unit(u, H, NT);
+            orow0 = grow(un, r0, T, H);
+        }
+        const size_t obase = orow0 * KD + d;
+        static_assert(KD == 128, "the db row below recovers orow0 as obase >> 7");
         const uint32_t hk = (uint32_t)H * KD;
 
         auto diag_row = [&](const int r) {
@@ -406,6 +497,7 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         // incoming gradients (ACCUM): fetched three output rows ahead of their use
         float inq[BC], ink[BC], ing[BC];
         auto fetch_in = [&](const int r) {
+            if (VARLEN && r0 + r >= ulen) return;
             if constexpr (ACCUM) {
                 const size_t off = obase + (size_t)((uint32_t)r * hk);
                 inq[r] = ex.dq_in ? __ldg(ex.dq_in + off) : 0.f;
@@ -419,6 +511,10 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             const int row = r0 + r;
             const size_t off = obase + (size_t)((uint32_t)r * hk);
             if (r >= 3) fetch_in(r - 3);
+            if (VARLEN && row >= ulen) {
+                dbv[r] = 0.f;
+                return;
+            }
             const float qv = to_f32(sq[row * KD + d]);
             const float kv = KDA_EL(k2, r), dkv = KDA_EL(dkt2, r);
             const float pk = sbeta[row] * acck[r];
@@ -470,7 +566,7 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
 #pragma unroll
         for (int r = BC - 1; r >= BC / 2; --r) {
             accq[r] = acck[r] = 0.f;
-            diag_row(r);
+            if (!VARLEN || r0 + r < ulen) diag_row(r);
         }
 
         // ---- cross terms: wait for the MMAs, apply the post-factors ----
@@ -528,15 +624,15 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         db_rows(BC / 2);
 #pragma unroll
         for (int r = BC / 2 - 1; r >= 0; --r) {
-            diag_row(r);
+            if (!VARLEN || r0 + r < ulen) diag_row(r);
             out_row(r);
         }
         db_rows(0);
 #undef KDA_EL
         tc::named_bar_sync(1 + i, 128);
-        if ((warp & 3) == 0 && lane < BC) {
+        if ((warp & 3) == 0 && lane < BC && (!VARLEN || r0 + lane < ulen)) {
             const int row = r0 + lane;
-            const size_t brow = grow(un, row, T, H);
+            const size_t brow = ((obase - (size_t)d) >> 7) + (size_t)((uint32_t)lane * (uint32_t)H);
             float v = (sdbp[row] + sdbp[BT + row]) + (sdbp[2 * BT + row] + sdbp[3 * BT + row]);
             if constexpr (ACCUM) {
                 if (ex.db_in) v += ex.db_in[brow];
@@ -556,7 +652,8 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
                 if (j > i) later += tot[j * KD + d];
 #pragma unroll
             for (int r = 0; r < BC; ++r)
-                dg[obase + (size_t)((uint32_t)r * hk)] = bank[(r0 + r) * KD + d] + later;
+                if (!VARLEN || r0 + r < ulen)
+                    dg[obase + (size_t)((uint32_t)r * hk)] = bank[(r0 + r) * KD + d] + later;
         }
 
         // ---- unit done: the last warp releases the stage and refills it ----
@@ -567,7 +664,8 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         prev = __shfl_sync(0xffffffffu, prev, 0);
         if ((prev % TC_WARPS) == TC_WARPS - 1 && u + 2 * stride < units) {
             tc::fence_proxy_async_smem();
-            load_unit(st, &full[sidx], tm, beta, u + 2 * stride, T, H, ex.G, lane);
+            load_unit<VARLEN>(st, &full[sidx], meta + 2 * sidx, tm, beta, u + 2 * stride, T, H,
+                              ex, lane);
         }
     }
 
@@ -585,9 +683,9 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
 cudaError_t make_maps(const BwdArgs &a, TmaMaps *tm);
 cudaError_t num_sms(int *n);
 
-template <typename io_t, bool ACCUM, bool FOLD, bool EMIT>
+template <typename io_t, bool ACCUM, bool FOLD, bool EMIT, bool VARLEN>
 cudaError_t launch_typed(const BwdArgs &a, cudaStream_t stream) {
-    auto kern = kda_intra_bwd_tc_kernel<io_t, ACCUM, FOLD, EMIT>;
+    auto kern = kda_intra_bwd_tc_kernel<io_t, ACCUM, FOLD, EMIT, VARLEN>;
     const int smem_bytes = FOLD ? SM_TOTAL_FOLD : SM_TOTAL;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
@@ -603,26 +701,33 @@ cudaError_t launch_typed(const BwdArgs &a, cudaStream_t stream) {
     ex.dg_in = a.dg_in;
     ex.db_in = a.db_in;
     ex.G = HV / a.H;
-    const long long units = (long long)a.B * HV * (a.T / BT);
+    ex.cu_seqlens = a.cu_seqlens;
+    ex.chunk_indices = a.chunk_indices;
+    ex.num_seqs = a.num_seqs;
+    const long long units =
+        VARLEN ? (long long)a.num_chunks * HV : (long long)a.B * HV * (a.T / BT);
+    if (units == 0) return cudaSuccess;
     const unsigned grid = (unsigned)(units < nsm ? units : nsm);
     kern<<<grid, TC_THREADS, smem_bytes, stream>>>(tm, a.beta, a.dq, a.dk, a.db, a.dg, a.T, HV,
                                                    units, ex);
     return cudaGetLastError();
 }
 
-template <typename io_t, bool EMIT>
+template <typename io_t, bool EMIT, bool VARLEN>
 cudaError_t launch_opts(const BwdArgs &a, cudaStream_t stream) {
     const bool accum = a.dq_in || a.dk_in || a.dg_in || a.db_in;
     if (accum)
-        return a.fold_dg ? launch_typed<io_t, true, true, EMIT>(a, stream)
-                         : launch_typed<io_t, true, false, EMIT>(a, stream);
-    return a.fold_dg ? launch_typed<io_t, false, true, EMIT>(a, stream)
-                     : launch_typed<io_t, false, false, EMIT>(a, stream);
+        return a.fold_dg ? launch_typed<io_t, true, true, EMIT, VARLEN>(a, stream)
+                         : launch_typed<io_t, true, false, EMIT, VARLEN>(a, stream);
+    return a.fold_dg ? launch_typed<io_t, false, true, EMIT, VARLEN>(a, stream)
+                     : launch_typed<io_t, false, false, EMIT, VARLEN>(a, stream);
 }
 
-template <typename io_t>
+// Every option combination of one q/k element type and one sequence layout.
+template <typename io_t, bool VARLEN>
 cudaError_t launch_io(const BwdArgs &a, cudaStream_t stream) {
-    return a.emit_io ? launch_opts<io_t, true>(a, stream) : launch_opts<io_t, false>(a, stream);
+    return a.emit_io ? launch_opts<io_t, true, VARLEN>(a, stream)
+                     : launch_opts<io_t, false, VARLEN>(a, stream);
 }
 
 }  // namespace tcimpl

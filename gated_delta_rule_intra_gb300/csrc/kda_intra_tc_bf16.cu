@@ -1,8 +1,8 @@
-// Instantiations of the tensor-core kernel for __nv_bfloat16 q/k.
+// Instantiations of the tensor-core kernel: __nv_bfloat16 q/k, fixed-length sequences.
 #include "kda_intra_tc.cuh"
 
 namespace kda {
 cudaError_t launch_tc_bf16(const BwdArgs &a, cudaStream_t stream) {
-    return tcimpl::launch_io<__nv_bfloat16>(a, stream);
+    return tcimpl::launch_io<__nv_bfloat16, false>(a, stream);
 }
 }  // namespace kda

@@ -1,8 +1,8 @@
-// Instantiations of the tensor-core kernel for __half q/k.
+// Instantiations of the tensor-core kernel: __half q/k, fixed-length sequences.
 #include "kda_intra_tc.cuh"
 
 namespace kda {
 cudaError_t launch_tc_fp16(const BwdArgs &a, cudaStream_t stream) {
-    return tcimpl::launch_io<__half>(a, stream);
+    return tcimpl::launch_io<__half, false>(a, stream);
 }
 }  // namespace kda

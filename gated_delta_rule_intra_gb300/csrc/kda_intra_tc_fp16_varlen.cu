@@ -1,0 +1,8 @@
+// Instantiations of the tensor-core kernel: __half q/k, variable-length sequences.
+#include "kda_intra_tc.cuh"
+
+namespace kda {
+cudaError_t launch_tc_fp16_varlen(const BwdArgs &a, cudaStream_t stream) {
+    return tcimpl::launch_io<__half, true>(a, stream);
+}
+}  // namespace kda

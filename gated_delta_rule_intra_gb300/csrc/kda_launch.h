@@ -17,6 +17,11 @@ struct BwdArgs {
     const float *dq_in = nullptr, *dk_in = nullptr, *dg_in = nullptr, *db_in = nullptr;
     bool fold_dg = false;  // dg as its inclusive reverse cumsum inside each chunk
     bool emit_io = false;  // dq, dk written in the q/k element type
+    // variable-length sequences packed along T (B == 1): sequence n holds tokens
+    // [cu_seqlens[n], cu_seqlens[n+1]); chunk c of the launch is chunk
+    // chunk_indices[2c+1] of sequence chunk_indices[2c]
+    const int *cu_seqlens = nullptr, *chunk_indices = nullptr;
+    int num_seqs = 0, num_chunks = 0;
 };
 
 // All-FP32 SIMT kernel (one CTA per unit).

@@ -167,6 +167,15 @@ __device__ __forceinline__ void tma_load_5d(void *dst, const void *tmap, int c0,
         "r"(smem_u32(mbar))
         : "memory");
 }
+__device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, int c0, int c1, int c2,
+                                            int c3, uint64_t *mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "r"(smem_u32(mbar))
+        : "memory");
+}
 // Arrive on an mbarrier once all of this thread's earlier cp.async copies have landed.
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t *mbar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(mbar))

@@ -26,9 +26,9 @@
  * it is the bwd_intra page's epilogue value times ln2.  A caller whose gate lives
  * in natural-log units (g_nat = g * ln2) gets dL/dg_nat as dg / ln2.
  *
- * Supported shapes: K = 128 (head dimension), chunk 64, fixed-length sequences with
- * T a multiple of 64 (the page's fast path; its varlen / odd-shape fallback does not
- * exist here and such calls are rejected).  g must be the inclusive chunk-local
+ * Supported shapes: K = 128 (head dimension), chunk 64; fixed-length sequences with
+ * T a multiple of 64, or (kda_intra_bwd_ex only) variable-length sequences packed
+ * along T and described by cu_seqlens.  g must be the inclusive chunk-local
  * cumulative sum of per-step log2 gates that are <= 0 (non-increasing inside each
  * chunk): every exponent the kernels evaluate is then <= 0.
  *
@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 2
+#define KDA_ABI_VERSION 3
 #define KDA_BT 64  /* chunk length */
 #define KDA_BC 16  /* sub-block length inside a chunk */
 #define KDA_K 128  /* head dimension */
@@ -70,7 +70,8 @@ typedef struct CUstream_st *kda_stream_t;
 typedef enum {
     KDA_OK = 0,
     KDA_ERR_NULL = 1,               /* a required pointer is NULL */
-    KDA_ERR_SHAPE = 2,              /* B,T,H <= 0, H > KDA_MAX_H, T % 64 != 0, too large */
+    KDA_ERR_SHAPE = 2,              /* B,T,H <= 0, H > KDA_MAX_H, T % 64 != 0, too large;
+                                       varlen: B != 1, num_seqs <= 0, num_chunks < 0 */
     KDA_ERR_DTYPE = 3,              /* qk_dtype not KDA_BF16 / KDA_FP16 */
     KDA_ERR_ALIGN = 4,              /* a pointer is not 16-byte aligned */
     KDA_ERR_CUDA = 5,               /* a CUDA runtime call or the launch failed */
@@ -143,6 +144,24 @@ kda_status_t kda_intra_bwd_host(const void *q, const void *k, const float *g,
  *   dqdk_io_dtype  1: dq and dk are written in qk_dtype (round to nearest) instead of
  *                  fp32 -- bitwise the cast of the fp32 result.  Not allowed with HV > H
  *                  (the grouped-head reduction that follows must see fp32 values).
+ *   cu_seqlens     variable-length sequences (the host wrapper's cu_seqlens /
+ *   chunk_indices  chunk_indices pair).  B must be 1 and T is the packed token count
+ *   num_seqs       (any T >= 1).  cu_seqlens: device int32 [num_seqs + 1], sequence n
+ *   num_chunks     is tokens [cu_seqlens[n], cu_seqlens[n+1]), 0 = cu_seqlens[0] <=
+ *                  ... <= cu_seqlens[num_seqs] <= T.  chunk_indices: device int32
+ *                  [num_chunks][2], entry c = (n, j) names chunk j of sequence n, i.e.
+ *                  tokens cu_seqlens[n] + 64j ... min(+64, cu_seqlens[n+1]) - 1; chunks
+ *                  restart at every sequence start, and a sequence's last chunk may be
+ *                  short.  Each unit is then (chunk entry, head); all per-chunk
+ *                  definitions above apply to the chunk's valid rows only (g is the
+ *                  cumsum restarted at each chunk start, dA rows are indexed from the
+ *                  chunk start, fold_dg folds over the valid rows).  Both pointers are
+ *                  NULL for fixed-length calls (chunk_indices may also be NULL when
+ *                  num_chunks == 0: nothing is launched); the rows of tokens that no entry names
+ *                  are left untouched.  The values are read on the device only: an
+ *                  entry that names no chunk of cu_seqlens (n out of range, j past the
+ *                  sequence's end, a sequence past T) is skipped, so no input value can
+ *                  make the kernel access memory outside the argument buffers.
  *
  * Runs on the tensor-core path (the same accuracy contract as kda_intra_bwd).
  */
@@ -154,6 +173,10 @@ typedef struct {
     const float *db_in;
     int fold_dg;
     int dqdk_io_dtype;
+    const int *cu_seqlens;
+    const int *chunk_indices;
+    int num_seqs;
+    int num_chunks;
 } kda_intra_bwd_opts_t;
 
 kda_status_t kda_intra_bwd_ex(const void *q, const void *k, const float *g,

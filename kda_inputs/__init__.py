@@ -100,6 +100,76 @@ def make_inputs(B: int, T: int, H: int, *, gate_lo: float = -0.5,
     return dict(q=q, k=k, g=g, beta=beta, dAqk=dAqk, dAkk=dAkk)
 
 
+def varlen_seqlens(total: int, *, seed: int = SEED0, min_len: int = 1,
+                   max_len: int = 8192) -> list:
+    """A seeded mix of sequence lengths summing to exactly ``total``: lengths drawn
+    log-uniformly in [min_len, max_len] (many short sequences, most tokens in long
+    ones), the last one cut to fit."""
+    gen = torch.Generator().manual_seed(int(seed))
+    lo, hi = torch.log(torch.tensor(float(min_len))), torch.log(torch.tensor(float(max_len)))
+    out, left = [], int(total)
+    while left > 0:
+        u = torch.rand((), generator=gen)
+        n = int(torch.exp(lo + (hi - lo) * u).round().clamp(min_len, max_len))
+        n = min(n, left)
+        out.append(n)
+        left -= n
+    return out
+
+
+def make_varlen_inputs(seqlens, H: int, *, gate_lo: float = -0.5,
+                       qk_dtype: torch.dtype = torch.bfloat16, seed: int = SEED0,
+                       k_dim: int = K, bt: int = BT, HQ: int | None = None):
+    """Packed variable-length inputs: B = 1, T = sum(seqlens), sequence n at tokens
+    [cu[n], cu[n+1]).  Same distributions as make_inputs; the gate cumsum and the dA
+    triangles restart at every chunk of every sequence (chunks start at the sequence
+    start, the last one may be short).  q and k get HQ heads (default H).
+    Returns (inputs, cu_seqlens) with cu_seqlens an int32 CPU tensor."""
+    lens = [int(n) for n in seqlens]
+    if any(n < 0 for n in lens):
+        raise ValueError("sequence lengths must be >= 0")
+    T = sum(lens)
+    HQ = H if HQ is None else HQ
+    gen = torch.Generator().manual_seed(int(seed))
+    f32 = torch.float32
+
+    def unit_rows(x):
+        return (x / x.norm(dim=-1, keepdim=True)).to(qk_dtype)
+
+    q = unit_rows(torch.randn(1, T, HQ, k_dim, generator=gen, dtype=f32))
+    k = unit_rows(torch.randn(1, T, HQ, k_dim, generator=gen, dtype=f32))
+    step = torch.rand(1, T, H, k_dim, generator=gen, dtype=f32) * gate_lo
+    beta = torch.rand(1, T, H, generator=gen, dtype=f32)
+    cu = torch.tensor([0] + lens, dtype=torch.int64).cumsum(0)
+    # in-chunk position of every token
+    pos = torch.empty(T, dtype=torch.int64)
+    g = torch.empty(1, T, H, k_dim, dtype=f32)
+    for a, b in zip(cu[:-1].tolist(), cu[1:].tolist()):
+        for c0 in range(a, b, bt):
+            c1 = min(c0 + bt, b)
+            pos[c0:c1] = torch.arange(c1 - c0)
+            g[:, c0:c1] = step[:, c0:c1].cumsum(dim=1, dtype=f32)
+    cols = torch.arange(bt).view(1, bt)
+    lower = (cols <= pos.view(T, 1)).to(f32).view(1, T, 1, bt)
+    strict = (cols < pos.view(T, 1)).to(f32).view(1, T, 1, bt)
+    dAqk = (torch.randn(1, T, H, bt, generator=gen, dtype=f32) * lower).contiguous()
+    dAkk = (torch.randn(1, T, H, bt, generator=gen, dtype=f32) * strict).contiguous()
+    inputs = dict(q=q, k=k, g=g.contiguous(), beta=beta, dAqk=dAqk, dAkk=dAkk)
+    return inputs, cu.to(torch.int32)
+
+
+# The variable-length workload: the headline's 32768 tokens x 16 heads, cut into a
+# seeded log-uniform mix of sequence lengths in [1, 8192].
+VARLEN_WORKLOAD = dict(name="varlen_T32768_H16", total=32768, H=16, gate_lo=-0.5,
+                       max_len=8192)
+
+
+def make_varlen_workload(seed: int = SEED0):
+    w = VARLEN_WORKLOAD
+    lens = varlen_seqlens(w["total"], seed=seed, max_len=w["max_len"])
+    return make_varlen_inputs(lens, w["H"], gate_lo=w["gate_lo"], seed=seed + 1)
+
+
 def make_config_inputs(idx: int, seed: int | None = None) -> dict:
     cfg = CONFIGS[idx]
     return make_inputs(cfg.B, cfg.T, cfg.H, gate_lo=cfg.gate_lo,

@@ -152,3 +152,54 @@ def intra_bwd_ex(q, k, g, beta, dAqk, dAkk, *, dq_in=None, dk_in=None, dg_in=Non
     if fold_dg:
         dg = chunk_reverse_cumsum(dg, bt)
     return dq, dk, db, dg
+
+
+def intra_bwd_varlen(q, k, g, beta, dAqk, dAkk, cu_seqlens, *, dq_in=None, dk_in=None,
+                     dg_in=None, db_in=None, fold_dg=False, bt: int = 64, nthreads: int = 0,
+                     lib=None):
+    """Variable-length sequences packed along T (B == 1), composed from intra_bwd_ex.
+
+    Reading (the bwd_intra page's host wrapper takes cu_seqlens / chunk_indices and
+    sends them to its fallback): chunks restart at every sequence start, so a
+    sequence's last chunk may be short, and every per-chunk definition holds over the
+    chunk's valid rows only.  Each sequence is padded to whole chunks with rows that
+    take no part in any sum (q = k = 0, beta = 0, zero dA rows, zero incoming
+    gradients; the gate held at the last valid row's value), solved as one
+    fixed-length problem and cut back to its own rows.  Rows of tokens outside every
+    sequence come back as NaN.
+    """
+    cu = [int(v) for v in np.asarray(cu_seqlens).reshape(-1)]
+    arrs = {n: _f64(v) for n, v in (("q", q), ("k", k), ("g", g), ("beta", beta),
+                                     ("dAqk", dAqk), ("dAkk", dAkk))}
+    ins = {n: (None if v is None else _f64(v)) for n, v in (("dq_in", dq_in), ("dk_in", dk_in),
+                                                            ("dg_in", dg_in), ("db_in", db_in))}
+    if arrs["q"].shape[0] != 1:
+        raise ValueError("variable-length inputs have B == 1")
+    T, HV = arrs["g"].shape[1], arrs["g"].shape[2]
+    K = arrs["q"].shape[3]
+    dq = np.full((1, T, HV, K), np.nan)
+    dk = np.full((1, T, HV, K), np.nan)
+    dg = np.full((1, T, HV, K), np.nan)
+    db = np.full((1, T, HV), np.nan)
+    for a, b in zip(cu[:-1], cu[1:]):
+        L = b - a
+        if L <= 0:
+            continue
+        Lp = -(-L // bt) * bt
+
+        def pad(x, edge=False):
+            if x is None:
+                return None
+            y = x[:, a:b]
+            fill = np.repeat(y[:, -1:], Lp - L, axis=1) if edge else \
+                np.zeros((1, Lp - L) + y.shape[2:])
+            return np.concatenate([y, fill], axis=1)
+
+        part = intra_bwd_ex(pad(arrs["q"]), pad(arrs["k"]), pad(arrs["g"], edge=True),
+                            pad(arrs["beta"]), pad(arrs["dAqk"]), pad(arrs["dAkk"]),
+                            dq_in=pad(ins["dq_in"]), dk_in=pad(ins["dk_in"]),
+                            dg_in=pad(ins["dg_in"]), db_in=pad(ins["db_in"]),
+                            fold_dg=fold_dg, bt=bt, nthreads=nthreads, lib=lib)
+        for out, x in zip((dq, dk, db, dg), part):
+            out[:, a:b] = x[:, :L]
+    return dq, dk, db, dg

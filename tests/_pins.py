@@ -94,6 +94,52 @@ def autograd_backward(inp, bt):
             t["g"].grad.numpy())
 
 
+def ragged_autograd_backward(inp, cu_seqlens, bt):
+    """dq, dk, db, dg of packed variable-length sequences (B == 1) from torch fp64
+    autograd of the separable forward written per chunk over its valid rows only:
+    chunks start at each sequence start, the last one of a sequence may be short.
+    No padding and nothing shared with the oracle's composition."""
+    t = {n: torch.tensor(np.asarray(v, dtype=np.float64), requires_grad=True)
+         for n, v in inp.items() if n in ("q", "k", "g", "beta")}
+    dAqk = torch.as_tensor(np.asarray(inp["dAqk"], dtype=np.float64))
+    dAkk = torch.as_tensor(np.asarray(inp["dAkk"], dtype=np.float64))
+    cu = [int(v) for v in np.asarray(cu_seqlens).reshape(-1)]
+    L = torch.zeros((), dtype=torch.float64)
+    for a, b in zip(cu[:-1], cu[1:]):
+        for c0 in range(a, b, bt):
+            m = min(c0 + bt, b) - c0
+            sl = slice(c0, c0 + m)
+            q, k, g = (t[n][0, sl].transpose(0, 1) for n in ("q", "k", "g"))  # [H, m, K]
+            beta = t["beta"][0, sl].transpose(0, 1)                             # [H, m]
+            lower = torch.tril(torch.ones(m, m, dtype=torch.float64))
+            strict = torch.tril(torch.ones(m, m, dtype=torch.float64), -1)
+            up, dn = torch.exp2(g), torch.exp2(-g)
+            Aqk = ((q * up) @ (k * dn).transpose(-1, -2)) * lower
+            Akk = beta.unsqueeze(-1) * ((k * up) @ (k * dn).transpose(-1, -2)) * strict
+            gq = dAqk[0, sl, :, :m].transpose(0, 1)  # [H, m, m]
+            gk = dAkk[0, sl, :, :m].transpose(0, 1)
+            L = L + (gq * Aqk).sum() + (gk * Akk).sum()
+    L.backward()
+    return (t["q"].grad.numpy(), t["k"].grad.numpy(), t["beta"].grad.numpy(),
+            t["g"].grad.numpy())
+
+
+def ragged_reverse_cumsum(x, cu_seqlens, bt):
+    """Inclusive reverse cumsum along tokens inside each (possibly short) chunk of
+    packed variable-length sequences, by explicit loops over tokens."""
+    x = np.asarray(x, dtype=np.float64)
+    out = np.array(x)
+    cu = [int(v) for v in np.asarray(cu_seqlens).reshape(-1)]
+    for a, b in zip(cu[:-1], cu[1:]):
+        for c0 in range(a, b, bt):
+            c1 = min(c0 + bt, b)
+            run = np.zeros(x.shape[2:])
+            for tkn in range(c1 - 1, c0 - 1, -1):
+                run = run + x[0, tkn]
+                out[0, tkn] = run
+    return out
+
+
 def rel_err(a, b):
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)

@@ -182,3 +182,49 @@ def test_ex_accepts_in_place_and_reaches_the_device(lib):
     # NULL options behave like kda_intra_bwd
     args = fake_args()[:-1]
     assert lib.kda_intra_bwd_ex(*args, None, ctypes.c_void_p(0)) in (ERR_CUDA, ERR_DEVICE)
+
+
+def varlen_ins(num_seqs=2, num_chunks=3, cu=BASE + 10 * SPAN, ci=BASE + 11 * SPAN):
+    return {"cu_seqlens": cu, "chunk_indices": ci, "num_seqs": num_seqs,
+            "num_chunks": num_chunks}
+
+
+def test_ex_varlen_rejections(lib):
+    assert ex_call(lib, B=2, T=128, ins=varlen_ins()) == ERR_SHAPE        # varlen needs B == 1
+    assert ex_call(lib, ins=varlen_ins(num_seqs=0)) == ERR_SHAPE
+    assert ex_call(lib, ins=varlen_ins(num_chunks=-1)) == ERR_SHAPE
+    assert ex_call(lib, T=0, ins=varlen_ins()) == ERR_SHAPE
+    assert ex_call(lib, H=1, HV=1 << 16, ins=varlen_ins(num_chunks=1 << 16)) == ERR_SHAPE
+    assert ex_call(lib, ins=varlen_ins(cu=0)) == ERR_NULL                  # table without offsets
+    assert ex_call(lib, ins=varlen_ins(ci=0)) == ERR_NULL                  # offsets, chunks, no table
+    assert ex_call(lib, ins=varlen_ins(cu=BASE + 10 * SPAN + 2)) == ERR_ALIGN
+    assert ex_call(lib, ins=varlen_ins(ci=BASE + 11 * SPAN + 1)) == ERR_ALIGN
+    # the offsets inside an output buffer
+    assert ex_call(lib, ins=varlen_ins(cu=BASE + 8 * SPAN + 16)) == ERR_OVERLAP
+    # a chunk table running into db
+    assert ex_call(lib, ins=varlen_ins(ci=BASE + 8 * SPAN - 8, num_chunks=2)) == ERR_OVERLAP
+    # and without varlen, T % 64 is still required
+    assert ex_call(lib, T=100) == ERR_SHAPE
+
+
+def test_ex_varlen_accepts_any_token_count(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("would launch on a real device")
+    for T in (1, 63, 100, 64 * 7 + 5):
+        assert ex_call(lib, T=T, ins=varlen_ins()) in (ERR_CUDA, ERR_DEVICE)
+    # an empty chunk table may be NULL
+    assert ex_call(lib, T=5, ins=varlen_ins(ci=0, num_chunks=0)) in (ERR_CUDA, ERR_DEVICE, 0)
+
+
+def test_prepare_chunk_indices():
+    import torch
+    cu = torch.tensor([0, 1, 64, 64, 193, 200], dtype=torch.int32)
+    ci = kda.prepare_chunk_indices(cu)
+    assert ci.dtype == torch.int32 and ci.shape == (6, 2)
+    assert ci.tolist() == [[0, 0], [1, 0], [3, 0], [3, 1], [3, 2], [4, 0]]
+    assert kda.prepare_chunk_indices(torch.tensor([0, 0])).shape == (0, 2)
+    with pytest.raises(ValueError):
+        kda.prepare_chunk_indices(torch.tensor([1, 5]))
+    with pytest.raises(ValueError):
+        kda.prepare_chunk_indices(torch.tensor([0, 5, 3]))

@@ -11,6 +11,9 @@ import oracle
 from tests import _pins
 
 
+_ARGS = ("q", "k", "g", "beta", "dAqk", "dAkk")
+
+
 @pytest.fixture(scope="module")
 def lib():
     return oracle.load()
@@ -135,3 +138,56 @@ def test_grouped_heads_with_one_group_is_the_plain_backward():
     b = oracle.intra_bwd_ex(*(inp[n] for n in ("q", "k", "g", "beta", "dAqk", "dAkk")), bt=8)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+# ------------------------------------------------------------ variable-length sequences
+
+VARLEN_LENS = [3, 8, 11, 1, 16, 5, 9]  # chunks of 8: short, whole, ragged, single row
+
+
+def _varlen_tiny(H=2, K=4, bt=8, seed=11, lens=VARLEN_LENS, gate_lo=-1.0, HQ=None):
+    x, cu = kda_inputs.make_varlen_inputs(lens, H, gate_lo=gate_lo, qk_dtype=torch.float32,
+                                          seed=seed, k_dim=K, bt=bt, HQ=HQ)
+    return {n: v.double().numpy() for n, v in x.items()}, cu.numpy()
+
+
+def test_varlen_against_ragged_autograd(lib):
+    """Short and ragged chunks against autograd of the per-chunk forward on the valid
+    rows only (the oracle pads; the pin does not)."""
+    inp, cu = _varlen_tiny()
+    got = oracle.intra_bwd_varlen(*(inp[n] for n in _ARGS), cu, bt=8, lib=lib)
+    want = _pins.ragged_autograd_backward(inp, cu, 8)
+    for name, a, b in zip(("dq", "dk", "db", "dg"), got, want):
+        assert _pins.rel_err(a, b) < 1e-12, name
+
+
+def test_varlen_options_against_ragged_autograd(lib):
+    """Grouped value heads, incoming gradients and the fold on ragged chunks."""
+    inp, cu = _varlen_tiny(H=4, HQ=2, seed=12, gate_lo=-3.0)
+    rng = np.random.default_rng(3)
+    T = inp["g"].shape[1]
+    ins = dict(dq_in=rng.standard_normal((1, T, 4, 4)), dk_in=rng.standard_normal((1, T, 4, 4)),
+               dg_in=rng.standard_normal((1, T, 4, 4)), db_in=rng.standard_normal((1, T, 4)))
+    got = oracle.intra_bwd_varlen(*(inp[n] for n in _ARGS), cu, fold_dg=True, bt=8, lib=lib,
+                                  **ins)
+    rep = dict(inp, q=np.repeat(inp["q"], 2, axis=2), k=np.repeat(inp["k"], 2, axis=2))
+    dq, dk, db, dg = _pins.ragged_autograd_backward(rep, cu, 8)
+    want = (dq + ins["dq_in"], dk + ins["dk_in"], db + ins["db_in"],
+            _pins.ragged_reverse_cumsum(dg + ins["dg_in"], cu, 8))
+    for name, a, b in zip(("dq", "dk", "db", "dg"), got, want):
+        assert _pins.rel_err(a, b) < 1e-12, name
+
+
+def test_varlen_whole_chunks_equal_the_fixed_length_oracle(lib):
+    """Sequences of whole chunks: the packed problem is the fixed-length one."""
+    inp, cu = _varlen_tiny(lens=[16, 8, 24], seed=13)
+    got = oracle.intra_bwd_varlen(*(inp[n] for n in _ARGS), cu, bt=8, lib=lib)
+    want = oracle.intra_bwd(*(inp[n] for n in _ARGS), bt=8, lib=lib)
+    for a, b in zip(got, want):
+        assert np.array_equal(a, b)
+
+
+def test_varlen_rows_outside_every_sequence_are_nan(lib):
+    inp, _ = _varlen_tiny(lens=[5, 7], seed=14)
+    got = oracle.intra_bwd_varlen(*(inp[n] for n in _ARGS), np.array([0, 5, 9]), bt=8, lib=lib)
+    assert np.isnan(got[0][0, 9:]).all() and np.isfinite(got[0][0, :9]).all()
