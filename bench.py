@@ -42,7 +42,10 @@ L2_BYTES = 129 * 2 ** 20
 KERNEL_NAMES = {
     "kda_intra_bwd": "kda_intra_bwd_tc_kernel",
     "kda_intra_bwd_fp32": "kda_intra_bwd_fp32_kernel",
+    "kda_intra_fwd": "kda_intra_fwd_tc_kernel",
 }
+# forward: q, k, g, beta in; Aqk, Akk ([64 x 64] fp32 each, zeros included) out
+FWD_BYTES_PER_UNIT = 2 * 64 * 128 * 2 + 64 * 128 * 4 + 64 * 4 + 2 * 64 * 64 * 4
 
 
 def algorithmic_bytes_per_unit(qk_bytes: int = 2, group: int = 1, accumulate: bool = False,
@@ -94,6 +97,7 @@ class VarlenWorkload:
 KERNEL_SOURCES = {
     "kda_intra_bwd_tc_kernel": ("kda_intra_tc.cuh", "kda_intra_tc.cu", "tc_ptx.cuh", "kda_common.cuh"),
     "kda_intra_bwd_fp32_kernel": ("kda_intra_fp32.cu", "kda_common.cuh"),
+    "kda_intra_fwd_tc_kernel": ("kda_intra_fwd_tc.cu", "tc_ptx.cuh", "kda_common.cuh"),
 }
 
 
@@ -241,6 +245,9 @@ def config_dict(cfg, path, opts=None):
         "l2": "no flush: inputs+outputs of one step (%.2f GB) exceed the 129 MB L2"
               % (cfg.units * algorithmic_bytes_per_unit() / 1e9),
     }
+    if path == "kda_intra_fwd":
+        d["l2"] = "no flush: inputs+outputs of one step (%.2f GB) exceed the 129 MB L2" % (
+            cfg.units * FWD_BYTES_PER_UNIT / 1e9)
     if opts:
         d["options"] = opts
     if isinstance(cfg, VarlenWorkload):
@@ -382,6 +389,11 @@ def run_ours(args, cfg):
         def step():
             kda.kda_intra_bwd_ex(*ins, *outs, **extra, fold_dg=args.fold_dg,
                                  dqdk_io_dtype=args.io_dtype_out, stream=stream)
+    elif args.path == "kda_intra_fwd":
+        outs = list(kda.kda_intra_fwd(*ins[:4]))
+
+        def step():
+            kda.kda_intra_fwd(*ins[:4], *outs, stream=stream)
     else:
         fn = getattr(kda, args.path)
         outs = kda._outputs(x["q"], None, None, None, None)
@@ -415,7 +427,8 @@ def run_ours(args, cfg):
 
     # end to end through the host-buffer entry point
     e2e = None
-    if not args.no_e2e and not extended:
+    fwd = args.path == "kda_intra_fwd"
+    if not args.no_e2e and not extended and not fwd:
         pin = {n: v.pin_memory() for n, v in cpu.items()}
         hout = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
         ws = torch.empty(kda.kda_intra_bwd_host_workspace_bytes(cfg.B, cfg.T, cfg.H,
@@ -444,7 +457,7 @@ def run_ours(args, cfg):
         del ws
 
     cpu_base = None
-    if world == 1 and rank == 0 and not args.no_cpu_baseline and not extended:
+    if world == 1 and rank == 0 and not args.no_cpu_baseline and not extended and not fwd:
         cpu_base = cpu_baseline(cpu, cfg)
         cpu_base["parity_check"] = sampled_check(cpu, cfg, outs)
 
@@ -457,6 +470,8 @@ def run_ours(args, cfg):
                                                     io_out=args.io_dtype_out)
         if args.gva > 1:
             bytes_per_launch -= cfg.T * cfg.H * 2 * kda_inputs.K * qk_bytes * (1 - 1 / args.gva)
+    elif fwd:
+        bytes_per_launch = cfg.units * FWD_BYTES_PER_UNIT
     else:
         bytes_per_launch = cfg.units * algorithmic_bytes_per_unit(
             qk_bytes, group=args.gva, accumulate=args.accumulate, io_out=args.io_dtype_out)

@@ -13,6 +13,7 @@ The functions carry the C names of ``include/kda.h``:
   the q/k dtype, variable-length sequences (``cu_seqlens``)
 * ``prepare_chunk_indices`` -- the (sequence, chunk) table of a ``cu_seqlens``
 * ``kda_intra_bwd_host``  -- host buffers in and out, copies on the stream
+* ``kda_intra_fwd``       -- the forward score matrices Aqk, Akk
 * ``kda_status_str``, ``kda_abi_version``
 """
 
@@ -72,6 +73,8 @@ def load_library(path: str | None = None):
     lib.kda_intra_bwd_ex.restype = st
     lib.kda_intra_bwd_host.argtypes = sig[:-1] + [vp, ctypes.c_size_t, vp]
     lib.kda_intra_bwd_host.restype = st
+    lib.kda_intra_fwd.argtypes = [vp, vp, fp, fp, fp, fp, i, i, i, i, vp]
+    lib.kda_intra_fwd.restype = st
     lib.kda_intra_bwd_host_workspace_bytes.argtypes = [i, i, i, i]
     lib.kda_intra_bwd_host_workspace_bytes.restype = ctypes.c_size_t
     lib.kda_status_str.argtypes = [i]
@@ -268,6 +271,34 @@ def kda_intra_bwd_ex(q, k, g, beta, dAqk, dAkk, dq=None, dk=None, db=None, dg=No
     if rc != KDA_OK:
         raise KdaError(rc, "kda_intra_bwd_ex")
     return dq, dk, db, dg
+
+
+def kda_intra_fwd(q, k, g, beta, Aqk=None, Akk=None, stream=None):
+    """Aqk, Akk ([B, T, H, 64] fp32, zeros outside the support) of the intra-chunk
+    forward on the CUDA tensors q, k ([B, T, H, 128] bf16/fp16), g ([B, T, H, 128]
+    fp32) and beta ([B, T, H] fp32)."""
+    if q.device.type != "cuda":
+        raise ValueError("kda_intra_fwd needs CUDA tensors (no CPU path exists)")
+    B, T, H = _shape(q)
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"q/k dtype must be bf16 or fp16, got {q.dtype}")
+    dev, f32 = q.device, torch.float32
+    Aqk = torch.empty(B, T, H, BT, device=dev, dtype=f32) if Aqk is None else Aqk
+    Akk = torch.empty(B, T, H, BT, device=dev, dtype=f32) if Akk is None else Akk
+    _check("k", k, (B, T, H, K), q.dtype, dev)
+    _check("g", g, (B, T, H, K), f32, dev)
+    _check("beta", beta, (B, T, H), f32, dev)
+    _check("Aqk", Aqk, (B, T, H, BT), f32, dev)
+    _check("Akk", Akk, (B, T, H, BT), f32, dev)
+    lib = load_library()
+    ptr = ctypes.c_void_p
+    with torch.cuda.device(dev):
+        rc = lib.kda_intra_fwd(ptr(q.data_ptr()), ptr(k.data_ptr()), ptr(g.data_ptr()),
+                               ptr(beta.data_ptr()), ptr(Aqk.data_ptr()), ptr(Akk.data_ptr()),
+                               B, T, H, _DTYPES[q.dtype], _stream_handle(stream, dev))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_intra_fwd")
+    return Aqk, Akk
 
 
 def kda_intra_bwd_host_workspace_bytes(B: int, T: int, H: int, qk_dtype=torch.bfloat16):

@@ -228,6 +228,41 @@ kda_status_t kda_intra_bwd(const void *q, const void *k, const float *g, const f
                                                                         : KDA_ERR_CUDA;
 }
 
+kda_status_t kda_intra_fwd(const void *q, const void *k, const float *g, const float *beta,
+                           float *Aqk, float *Akk, int B, int T, int H, kda_dtype_t qk_dtype,
+                           kda_stream_t stream) {
+    if (!q || !k || !g || !beta || !Aqk || !Akk) return KDA_ERR_NULL;
+    kda_status_t st = check_shape(B, T, H);
+    if (st != KDA_OK) return st;
+    if (qk_dtype != KDA_BF16 && qk_dtype != KDA_FP16) return KDA_ERR_DTYPE;
+    const void *a16[] = {q, k, g, Aqk, Akk};
+    for (const void *p : a16)
+        if ((uintptr_t)p % 16u) return KDA_ERR_ALIGN;
+    if ((uintptr_t)beta % 4u) return KDA_ERR_ALIGN;
+    const size_t rows = (size_t)B * T * H;
+    const Range in[] = {
+        {(uintptr_t)q, (uintptr_t)q + rows * KDA_K * 2},
+        {(uintptr_t)k, (uintptr_t)k + rows * KDA_K * 2},
+        {(uintptr_t)g, (uintptr_t)g + rows * KDA_K * 4},
+        {(uintptr_t)beta, (uintptr_t)beta + rows * 4},
+    };
+    const Range out[] = {
+        {(uintptr_t)Aqk, (uintptr_t)Aqk + rows * KDA_BT * 4},
+        {(uintptr_t)Akk, (uintptr_t)Akk + rows * KDA_BT * 4},
+    };
+    for (const Range &o : out)
+        for (const Range &r : in)
+            if (overlaps(o, r)) return KDA_ERR_OVERLAP;
+    if (overlaps(out[0], out[1])) return KDA_ERR_OVERLAP;
+    if ((st = check_device()) != KDA_OK) return st;
+    (void)cudaGetLastError();
+    kda::FwdArgs a;
+    a.q = q; a.k = k; a.g = g; a.beta = beta; a.Aqk = Aqk; a.Akk = Akk;
+    a.B = B; a.T = T; a.H = H;
+    a.fp16 = (qk_dtype == KDA_FP16);
+    return kda::launch_intra_fwd(a, (cudaStream_t)stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 size_t kda_intra_bwd_host_workspace_bytes(int B, int T, int H, kda_dtype_t qk_dtype) {
     if (check_shape(B, T, H) != KDA_OK) return 0;
     if (qk_dtype != KDA_BF16 && qk_dtype != KDA_FP16) return 0;

@@ -1,0 +1,455 @@
+// Tensor-core kernel for the KDA intra-chunk forward (sm_103a, tcgen05 + TMEM + TMA):
+// the two score matrices of every unit (b, h, 64-token chunk),
+//     Aqk[r,s] = sum_d q[r,d] k[s,d] 2^(g[r,d] - g[s,d])            (s <= r)
+//     Akk[r,s] = beta[r] sum_d k[r,d] k[s,d] 2^(g[r,d] - g[s,d])    (s <  r)
+// (bwd_intra page, module docstring: the forward whose gradient the backward takes),
+// written as [B,T,H,64] fp32 rows with zeros outside the support.
+//
+// Persistent grid, one 512-thread CTA per SM, two TMA input stages.  Per unit:
+//  * cross-sub-block blocks (r in block t, s in block j < t) through the target
+//    block's first row: 2^(g_r - g_s) = 2^(g_r - g_16t) * 2^(g_16t - g_s), both
+//    exponents <= 0 (the gate-magnitude law).  A[m, d] = q_r 2^(g_r - g_16t) for
+//    TMEM lane m = r and beta_r k_r 2^(g_r - g_16t) for lane m = 64 + r (written by
+//    tcgen05.st from the thread owning the lane); B_t[s, d] = k_s 2^(g_16t - g_s)
+//    for s < 16t in shared memory.  Three TF32 MMA chains (N = 16t, K = 128) give
+//    every cross entry of Aqk (lanes 0..63) and Akk (lanes 64..127) at once.
+//  * diagonal 16x16 blocks on the FP32 pipes with one exp2 per (r, s, d): thread
+//    (row pair {a, 15-a} of block i, 8 channels) sums over its channels, then a
+//    transposed shuffle reduction over the 16 lanes of its half-warp finishes the
+//    sum over d.
+//  * both tiles are assembled in a 128B-swizzled staging buffer whose entries
+//    outside the support stay zero, and leave through four TMA stores.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kda_common.cuh"
+#include "kda_launch.h"
+#include "tc_ptx.cuh"
+
+namespace kda {
+namespace fwdimpl {
+namespace {
+
+constexpr int FW_THREADS = 512;
+constexpr uint32_t SPIN_LIMIT = 1u << 22;
+
+// ---- shared memory (offsets from a 1024-byte aligned base) ----
+// Input stage: q, k as two 8 KB boxes each (64 rows x 64 elements = 128 B rows), g as
+// four 8 KB boxes (64 rows x 32 floats); every box is 128B-swizzled: the 16-byte chunk
+// c of row r sits at chunk position c ^ (r % 8) of the row's 128 bytes.
+constexpr int FS_Q = 0;
+constexpr int FS_K = 16384;
+constexpr int FS_G = 32768;
+constexpr int FSTAGE = 65536;
+constexpr int FM_STG = 2 * FSTAGE;              // Aqk, Akk tiles: 2 x 2 swizzled 8 KB boxes
+constexpr int FM_B = FM_STG + 32768;            // B_1, B_2, B_3: [16t][128] tf32, K-major
+constexpr int FM_BETA = FM_B + 49152;           // f32 [2][64]
+constexpr int FM_BAR = FM_BETA + 512;           // full[2], mma
+constexpr int FM_TSLOT = FM_BAR + 24;
+constexpr int FM_TOTAL = FM_TSLOT + 8;
+constexpr int FM_ALLOC = FM_TOTAL + 1024;       // slack for aligning the base
+static_assert(FM_STG % 1024 == 0, "swizzled staging needs 1024-byte alignment");
+static_assert(FM_ALLOC <= 232448, "shared memory");
+
+constexpr uint32_t FSTAGE_TX_BYTES = 2 * BT * KD * 2 + BT * KD * 4;
+constexpr uint32_t FULL_ARRIVALS = 1 + 32;
+
+// B_t at FM_B + boff(t): element (n, k) at (k/4)*256t + (n/8)*128 + (n%8)*16 + (k%4)*4
+__host__ __device__ constexpr int boff(int t) { return 4096 * t * (t - 1); }
+// TMEM: A in columns 0..127, D_t (16t columns) at tm_d(t)
+__device__ __forceinline__ uint32_t tm_d(int t) { return 128u + 8u * (uint32_t)(t * (t - 1)); }
+constexpr uint32_t TM_COLS = 256;
+
+// byte offset of element (r, c) of a swizzled tile made of 128-byte-row boxes
+template <int ESIZE>
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+    constexpr int PER_ROW = 128 / ESIZE;  // elements per box row
+    const int box = c / PER_ROW, cc = c % PER_ROW;
+    const int chunk = (cc * ESIZE) >> 4, within = (cc * ESIZE) & 15;
+    return (uint32_t)(box * 8192 + r * 128 + ((chunk ^ (r & 7)) << 4) + within);
+}
+// staging: tensor 0 = Aqk, 1 = Akk; column s in box s / 32
+__device__ __forceinline__ uint32_t stg_off(int tensor, int r, int s) {
+    return (uint32_t)(tensor * 16384) + swz<4>(r, s);
+}
+
+struct FwdMaps {
+    CUtensorMap q, k, g, aqk, akk;
+};
+
+// One warp queues a unit's copies: 8 swizzled TMA boxes from lane 0, beta as 64
+// four-byte cp.async copies from all lanes.
+template <typename io_t>
+__device__ __forceinline__ void load_unit(unsigned char *st, float *sbeta, uint64_t *full,
+                                          const FwdMaps &tm, const float *__restrict__ beta,
+                                          long long u, int T, int H, int lane) {
+    const Unit x = decode_unit(u, H, T / BT);
+    const int row = x.b * T + x.c * BT;
+    if (lane == 0) {
+        tc::mbar_arrive_expect_tx(full, FSTAGE_TX_BYTES);
+        for (int b = 0; b < 2; ++b) {
+            tc::tma_load_3d(st + FS_Q + b * 8192, &tm.q, 64 * b, x.h, row, full);
+            tc::tma_load_3d(st + FS_K + b * 8192, &tm.k, 64 * b, x.h, row, full);
+        }
+        for (int b = 0; b < 4; ++b) tc::tma_load_3d(st + FS_G + b * 8192, &tm.g, 32 * b, x.h, row, full);
+    }
+    const float *b0 = beta + ((size_t)row * H + x.h);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int r = lane + 32 * e;
+        const uint32_t s = tc::smem_u32(sbeta + r);
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(b0 + (size_t)r * H)
+                     : "memory");
+    }
+    tc::cp_async_mbar_arrive_noinc(full);
+}
+
+// Sum of v[0..15] over the 16 lanes of a half-warp, transposed: lane (lane & 15) = j
+// ends with the total of index j in v[0].  15 shuffles.
+__device__ __forceinline__ float reduce16(float (&v)[16], int lane) {
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1) {
+        const bool hi = (lane & w) != 0;
+#pragma unroll
+        for (int j = 0; j < w; ++j) {
+            const float send = hi ? v[j] : v[j + w];
+            const float keep = hi ? v[j + w] : v[j];
+            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        }
+    }
+    return v[0];
+}
+
+// Eight channels {4c..4c+3, 64+4c..64+4c+3} of one row of a swizzled stage tile.
+template <typename io_t>
+__device__ __forceinline__ void ld8_io(const unsigned char *tile, int r, int c, float2 (&x)[4]) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint2 w = *reinterpret_cast<const uint2 *>(tile + swz<2>(r, 64 * h + 4 * c));
+        const io_t *e = reinterpret_cast<const io_t *>(&w);
+        x[2 * h] = make_float2(to_f32(e[0]), to_f32(e[1]));
+        x[2 * h + 1] = make_float2(to_f32(e[2]), to_f32(e[3]));
+    }
+}
+__device__ __forceinline__ void ld8_f32(const unsigned char *tile, int r, int c, float2 (&x)[4]) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float4 w = *reinterpret_cast<const float4 *>(tile + swz<4>(r, 64 * h + 4 * c));
+        x[2 * h] = make_float2(w.x, w.y);
+        x[2 * h + 1] = make_float2(w.z, w.w);
+    }
+}
+
+template <typename io_t>
+__global__ void __launch_bounds__(FW_THREADS, 1)
+kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restrict__ beta,
+                        int T, int H, long long units) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem =
+        smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);  // 1024-aligned
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + FM_BAR);
+    uint64_t *mbar = full + 2;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + FM_TSLOT);
+    unsigned char *stg = smem + FM_STG;
+    const long long stride = gridDim.x;
+
+    if (warp == 0) tc::tmem_alloc(tslot, TM_COLS);
+    if (tid == 0) {
+        tc::mbar_init(&full[0], FULL_ARRIVALS);
+        tc::mbar_init(&full[1], FULL_ARRIVALS);
+        tc::mbar_init(mbar, 1);
+        tc::prefetch_tmap(&tm.q);
+        tc::prefetch_tmap(&tm.k);
+        tc::prefetch_tmap(&tm.g);
+        tc::prefetch_tmap(&tm.aqk);
+        tc::prefetch_tmap(&tm.akk);
+    }
+    // the staging entries outside the support are never written again: zero them once
+    for (int x = tid; x < 32768 / 16; x += FW_THREADS)
+        reinterpret_cast<uint4 *>(stg)[x] = make_uint4(0u, 0u, 0u, 0u);
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tbase = *tslot;
+
+    if (warp == 0) {
+        const long long u0 = blockIdx.x;
+        float *sb = reinterpret_cast<float *>(smem + FM_BETA);
+        if (u0 < units) load_unit<io_t>(smem, sb, &full[0], tm, beta, u0, T, H, lane);
+        if (u0 + stride < units)
+            load_unit<io_t>(smem + FSTAGE, sb + 64, &full[1], tm, beta, u0 + stride, T, H, lane);
+    }
+
+    const float nan = __int_as_float(0x7fc00000);
+    bool ok = true;
+    int it = 0;
+    for (long long u = blockIdx.x; u < units; u += stride, ++it) {
+        const int sidx = it & 1;
+        unsigned char *st = smem + sidx * FSTAGE;
+        const unsigned char *sq = st + FS_Q, *sk = st + FS_K, *sg = st + FS_G;
+        const float *sbeta = reinterpret_cast<const float *>(smem + FM_BETA) + 64 * sidx;
+        ok &= tc::mbar_wait(&full[sidx], (uint32_t)(it >> 1) & 1u, SPIN_LIMIT);
+
+        // ---- prescale: thread = (TMEM lane m, 32 channels).  Lane m < 64 holds the q
+        // row m, lane m >= 64 the beta*k row m - 64 (A operand); k rows also build the
+        // B operands of every later target block. ----
+        {
+            const int Lq = warp & 3, d0 = 32 * (warp >> 2);
+            const bool isk = Lq >= 2;
+            const int r = 32 * (Lq & 1) + lane, t = r >> 4;
+            const unsigned char *sx = isk ? sk : sq;
+            const float scale = isk ? sbeta[r] : 1.f;
+            const uint32_t tl = tbase + ((uint32_t)(32 * Lq) << 16);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float v[16];
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {  // 8 channels per 16-byte chunk of x
+                    const int ch = d0 + 16 * h + 8 * c;
+                    const uint4 w = *reinterpret_cast<const uint4 *>(sx + swz<2>(r, ch));
+                    const io_t *e = reinterpret_cast<const io_t *>(&w);
+#pragma unroll
+                    for (int q4 = 0; q4 < 2; ++q4) {
+                        const float4 gr = *reinterpret_cast<const float4 *>(sg + swz<4>(r, ch + 4 * q4));
+                        const float4 gb =
+                            *reinterpret_cast<const float4 *>(sg + swz<4>(16 * t, ch + 4 * q4));
+                        const int o = 8 * c + 4 * q4;
+                        v[o + 0] = to_f32(e[4 * q4 + 0]) * scale * ex2(gr.x - gb.x);
+                        v[o + 1] = to_f32(e[4 * q4 + 1]) * scale * ex2(gr.y - gb.y);
+                        v[o + 2] = to_f32(e[4 * q4 + 2]) * scale * ex2(gr.z - gb.z);
+                        v[o + 3] = to_f32(e[4 * q4 + 3]) * scale * ex2(gr.w - gb.w);
+                    }
+                }
+                tc::tmem_st16(tl + (uint32_t)(d0 + 16 * h), v);
+            }
+            if (isk && t < NBLK - 1) {
+                // B_tt[s = r, d] = k_r 2^(g_e - g_r) 2^(g_16tt - g_e), e = 16(t+1), tt > t
+                const int e = BC * (t + 1);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const int ch = d0 + 4 * q4;
+                    const uint2 w = *reinterpret_cast<const uint2 *>(sk + swz<2>(r, ch));
+                    const io_t *kk = reinterpret_cast<const io_t *>(&w);
+                    const float4 gs = *reinterpret_cast<const float4 *>(sg + swz<4>(r, ch));
+                    const float4 ge = *reinterpret_cast<const float4 *>(sg + swz<4>(e, ch));
+                    float4 a = make_float4(to_f32(kk[0]) * ex2(ge.x - gs.x),
+                                           to_f32(kk[1]) * ex2(ge.y - gs.y),
+                                           to_f32(kk[2]) * ex2(ge.z - gs.z),
+                                           to_f32(kk[3]) * ex2(ge.w - gs.w));
+                    const uint32_t nofs = (uint32_t)((r >> 3) * 128 + (r & 7) * 16);
+                    for (int tt = t + 1; tt < NBLK; ++tt) {
+                        float4 o = a;
+                        if (tt > t + 1) {
+                            const float4 gt =
+                                *reinterpret_cast<const float4 *>(sg + swz<4>(BC * tt, ch));
+                            o = make_float4(a.x * ex2(gt.x - ge.x), a.y * ex2(gt.y - ge.y),
+                                            a.z * ex2(gt.z - ge.z), a.w * ex2(gt.w - ge.w));
+                        }
+                        *reinterpret_cast<float4 *>(smem + FM_B + boff(tt) + (ch >> 2) * 256 * tt +
+                                                    nofs) = o;
+                    }
+                }
+            }
+        }
+        tc::tmem_wait_st();
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        if (tid == 0) tc::bulk_wait_read_all();  // the last unit's tiles have left the staging
+        __syncthreads();
+        tc::fence_after_sync();
+        if (warp == 0) {
+            if (tc::elect_one()) {
+#pragma unroll
+                for (int t = 1; t < NBLK; ++t) {
+                    const uint64_t b0 =
+                        tc::smem_desc(tc::smem_u32(smem + FM_B + boff(t)), 256 * t, 128);
+                    const uint32_t id = tc::idesc_tf32(128, 16 * t);
+#pragma unroll
+                    for (int kk = 0; kk < KD / 8; ++kk)
+                        tc::mma_tf32_ts(tbase + tm_d(t), tbase + 8 * kk,
+                                        b0 + (uint64_t)((512 * t * kk) >> 4), id, kk > 0);
+                }
+                tc::mma_commit(mbar);
+            }
+            __syncwarp();
+        }
+
+        // ---- diagonal blocks: thread = (block i, rows {a, 15-a}, channel group c).
+        // Row r meets sources s = 16i + s0 .. 16i + s0 + 7 (those with s <= r) in one
+        // call; the half-warp's 16 lanes then reduce [Aqk sums, Akk sums] over their
+        // channel groups, and lane c writes entry s0 + (c % 8) of Aqk (c < 8) or Akk. ----
+        {
+            const int i = warp >> 2;
+            const int a = 2 * (warp & 3) + (lane >> 4);
+            const int c = lane & 15;
+            const float2 neg1 = make_float2(-1.f, -1.f);
+            auto diag8 = [&](const int r, const int s0) {
+                const int last = r - BC * i;  // in-block index of the diagonal source
+                float2 qv[4], kv[4], gv[4];
+                ld8_io<io_t>(sq, r, c, qv);
+                ld8_io<io_t>(sk, r, c, kv);
+                ld8_f32(sg, r, c, gv);
+                float v[16];
+#pragma unroll
+                for (int sl = 0; sl < 8; ++sl) {
+                    v[sl] = v[8 + sl] = 0.f;
+                    // keep the loads of at most two sources in flight (register budget)
+                    if ((sl & 1) == 0) asm volatile("" ::: "memory");
+                    if (s0 + sl <= last) {
+                        float2 ks[4], gs[4];
+                        ld8_io<io_t>(sk, BC * i + s0 + sl, c, ks);
+                        ld8_f32(sg, BC * i + s0 + sl, c, gs);
+                        float2 pq = make_float2(0.f, 0.f), pk = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            const float2 df = __ffma2_rn(gs[x], neg1, gv[x]);
+                            const float2 tq = __fmul2_rn(ks[x], make_float2(ex2(df.x), ex2(df.y)));
+                            pq = __ffma2_rn(qv[x], tq, pq);
+                            pk = __ffma2_rn(kv[x], tq, pk);
+                        }
+                        v[sl] = pq.x + pq.y;
+                        v[8 + sl] = pk.x + pk.y;
+                    }
+                }
+                float sum = reduce16(v, lane);
+                const int sc = s0 + (c & 7);
+                if (c >= 8) sum *= sbeta[r];
+                if (!ok) sum = nan;
+                if (c < 8 ? sc <= last : sc < last)
+                    *reinterpret_cast<float *>(stg + stg_off(c >> 3, r, BC * i + sc)) = sum;
+            };
+            diag8(BC * i + BC - 1 - a, 0);
+            diag8(BC * i + BC - 1 - a, 8);
+            diag8(BC * i + a, 0);
+        }
+
+        // ---- cross blocks: TMEM lane m -> row r of Aqk (m < 64) or Akk (m >= 64),
+        // warp (Lq, Dq) takes the 16 source columns 16Dq.. of its lanes' target block ----
+        ok &= tc::mbar_wait(mbar, (uint32_t)it & 1u, SPIN_LIMIT);
+        tc::fence_after_sync();
+        {
+            const int Lq = warp & 3, Dq = warp >> 2;
+            const int r = 32 * (Lq & 1) + lane, tensor = Lq >> 1;
+            const int t_lo = 2 * (Lq & 1), t_hi = t_lo + 1;  // blocks of lanes 0-15, 16-31
+            const uint32_t tl = tbase + ((uint32_t)(32 * Lq) << 16);
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                const int t = part ? t_lo : t_hi;
+                if (Dq < t) {  // warp-uniform
+                    float v[16];
+                    tc::tmem_ld16(tl + tm_d(t) + 16 * Dq, v);
+                    tc::tmem_wait_ld();
+                    if ((lane >> 4) == (part ? 0 : 1)) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            float4 o = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2],
+                                                   v[4 * q4 + 3]);
+                            if (!ok) o = make_float4(nan, nan, nan, nan);
+                            *reinterpret_cast<float4 *>(stg + stg_off(tensor, r, 16 * Dq + 4 * q4)) = o;
+                        }
+                    }
+                }
+            }
+        }
+
+        // ---- unit done: tiles out through TMA, stage refilled ----
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (tid == 0) {
+            const Unit x = decode_unit(u, H, T / BT);
+            const int row = x.b * T + x.c * BT;
+            tc::tma_store_3d(&tm.aqk, stg, 0, x.h, row);
+            tc::tma_store_3d(&tm.aqk, stg + 8192, 32, x.h, row);
+            tc::tma_store_3d(&tm.akk, stg + 16384, 0, x.h, row);
+            tc::tma_store_3d(&tm.akk, stg + 24576, 32, x.h, row);
+            tc::bulk_commit_group();
+        }
+        if (warp == 0 && u + 2 * stride < units)
+            load_unit<io_t>(st, reinterpret_cast<float *>(smem + FM_BETA) + 64 * sidx, &full[sidx],
+                            tm, beta, u + 2 * stride, T, H, lane);
+    }
+
+    if (tid == 0) tc::bulk_wait_all();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tbase, TM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+int g_num_sms[64];
+
+cudaError_t get_encoder() {
+    if (g_encode) return cudaSuccess;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return cudaSuccess;
+}
+
+// 3-d map (element, head, token row) with a 64-row box of 128-byte rows, 128B swizzle
+cudaError_t encode_rows(CUtensorMap *m, CUtensorMapDataType dt, int esize, const void *base,
+                        cuuint64_t width, cuuint64_t heads, cuuint64_t rows) {
+    const cuuint64_t dims[3] = {width, heads, rows};
+    const cuuint64_t str[2] = {width * esize, heads * width * esize};
+    const cuuint32_t box[3] = {(cuuint32_t)(128 / esize), 1, BT};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, dt, 3, const_cast<void *>(base), dims, str, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <typename io_t>
+cudaError_t launch_typed(const FwdArgs &a, cudaStream_t stream) {
+    auto kern = kda_intra_fwd_tc_kernel<io_t>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         FM_ALLOC);
+    if (e != cudaSuccess) return e;
+    if ((e = get_encoder()) != cudaSuccess) return e;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    int nsm = (dev >= 0 && dev < 64) ? g_num_sms[dev] : 0;
+    if (nsm == 0) {
+        if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return e;
+        if (dev >= 0 && dev < 64) g_num_sms[dev] = nsm;
+    }
+    const cuuint64_t rows = (cuuint64_t)a.B * a.T, H = (cuuint64_t)a.H;
+    const CUtensorMapDataType io =
+        a.fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    FwdMaps tm;
+    if ((e = encode_rows(&tm.q, io, 2, a.q, KD, H, rows)) != cudaSuccess ||
+        (e = encode_rows(&tm.k, io, 2, a.k, KD, H, rows)) != cudaSuccess ||
+        (e = encode_rows(&tm.g, f32, 4, a.g, KD, H, rows)) != cudaSuccess ||
+        (e = encode_rows(&tm.aqk, f32, 4, a.Aqk, BT, H, rows)) != cudaSuccess ||
+        (e = encode_rows(&tm.akk, f32, 4, a.Akk, BT, H, rows)) != cudaSuccess)
+        return e;
+    const long long units = (long long)a.B * a.H * (a.T / BT);
+    const unsigned grid = (unsigned)(units < nsm ? units : nsm);
+    kern<<<grid, FW_THREADS, FM_ALLOC, stream>>>(tm, a.beta, a.T, a.H, units);
+    return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace fwdimpl
+
+cudaError_t launch_intra_fwd(const FwdArgs &a, cudaStream_t stream) {
+    return a.fp16 ? fwdimpl::launch_typed<__half>(a, stream)
+                  : fwdimpl::launch_typed<__nv_bfloat16>(a, stream);
+}
+
+}  // namespace kda

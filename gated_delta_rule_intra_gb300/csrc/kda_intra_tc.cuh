@@ -69,7 +69,9 @@ constexpr int SM_MMA = SM_FULL + 16;         // MMAs-done mbarrier
 constexpr int SM_CNT = SM_MMA + 8;           // operand counter, unit-done counter
 constexpr int SM_TSLOT = SM_CNT + 8;
 constexpr int SM_META = SM_TSLOT + 8;        // varlen: per stage {first token row, valid rows}
-constexpr int SM_TOTAL = SM_META + 16;
+constexpr int SM_PEND = SM_META + 16;        // varlen: the same for the unit after next
+constexpr int SM_VPIPE = SM_PEND + 16;       // varlen: chunk-table lookup in flight
+constexpr int SM_TOTAL = SM_VPIPE + 16;
 // extra shared memory of the fold_dg variant: the per-row dg bank [64][128] and the
 // per-(sub-block, channel) totals, double-buffered by unit parity
 constexpr int SM_FOLD_BANK = (SM_TOTAL + 127) / 128 * 128;
@@ -166,20 +168,32 @@ __device__ __forceinline__ void cp_async4_zfill(void *smem, const void *gmem, bo
 // tensor map can describe it when H is not a multiple of 4).  A variable-length unit
 // may start at any token row: its dA tiles come through the 4-d map (any row start),
 // rows past the sequence's end are loaded as they are (or zero-filled past the
-// tensor's end) and masked by the consumer, and their beta is zero-filled.  Lane 0
-// records the unit's row range in `meta` before its arrival on the stage barrier,
-// which publishes it with the data.
+// tensor's end) and masked by the consumer, and their beta is zero-filled.  Its row
+// range comes from `known` ({first row, valid rows}, read by lane 0 and broadcast)
+// when given, else from the chunk table.  Lane 0 records it in `meta` before its
+// arrival on the stage barrier, which publishes it with the data.
 template <bool VARLEN>
 __device__ __forceinline__ void load_unit(unsigned char *st, uint64_t *full, int *meta,
                                           const TmaMaps &tm, const float *__restrict__ beta,
                                           long long u, int T, int H, const Extras ex,
-                                          int lane) {
+                                          int lane, const int *known = nullptr) {
     int row, h, len = BT;  // first token row of the unit, head, valid rows
     if constexpr (VARLEN) {
-        const VarUnit x = varlen_unit(u, H, T, ex);
-        row = x.start;
-        len = x.len;
-        h = x.h;
+        if (known) {
+            int a = 0, b = 0;
+            if (lane == 0) {
+                a = known[0];
+                b = known[1];
+            }
+            row = __shfl_sync(0xffffffffu, a, 0);
+            len = __shfl_sync(0xffffffffu, b, 0);
+            h = (int)((unsigned)u % (unsigned)H);
+        } else {
+            const VarUnit x = varlen_unit(u, H, T, ex);
+            row = x.start;
+            len = x.len;
+            h = x.h;
+        }
         if (lane == 0) {
             meta[0] = row;
             meta[1] = len;
@@ -228,9 +242,10 @@ __device__ __forceinline__ void load_unit(unsigned char *st, uint64_t *full, int
 // ACCUM: add the optional incoming gradients of Extras; FOLD: return dg as its
 // inclusive reverse cumsum inside each chunk; EMIT: store dq and dk as io_t;
 // VARLEN: units come from cu_seqlens / chunk_indices, and a unit's rows past its
-// sequence's end (row >= len) are masked: their q, k and beta read as 0, their gate
-// as the last valid row's (so every exponent stays <= 0), their dA rows take no part
-// in the column-side sums, and nothing is written for them.
+// sequence's end (row >= len, "foreign" rows) are masked: their q, k, beta and
+// diagonal-block dA rows read as 0, their gate as the last valid row's (so every
+// exponent stays <= 0), their off-diagonal dA rows are zeroed in the column-side
+// operands, and nothing is stored for them.
 template <typename io_t, bool ACCUM, bool FOLD, bool EMIT, bool VARLEN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restrict__ beta,
@@ -295,8 +310,49 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         // valid rows of this unit and the last of them (rows past it take its gate)
         int ulen = BT;
         if constexpr (VARLEN) ulen = meta[2 * sidx + 1];
-        const int glast = ulen > 0 ? ulen - 1 : 0;
-        auto grow_g = [&](const int r) { return VARLEN ? min(r, glast) : r; };
+        const bool partial = VARLEN && ulen < BT;
+        // rows past the end take the last valid row's gate
+        const float glastv = partial ? sg[(ulen > 0 ? ulen - 1 : 0) * KD + d] : 0.f;
+        auto gsel = [&](const int r, const float v) { return (partial && r >= ulen) ? glastv : v; };
+
+        // VARLEN, chunk shorter than 64 rows: each sub-block group zeroes its foreign
+        // rows (row >= len) of q and of its diagonal dA blocks, the only stage data its
+        // rows read without a register-side mask, so the diagonal and epilogue rows run
+        // unguarded and foreign rows contribute exact zeros.  k, beta and g are masked
+        // in registers / at load (below).
+        if (partial) {
+            {
+                const int f = (d & 63) * 4;  // float4 of the diagonal block, row n
+                const int n = ((f >> 5) & 1) * 8 + ((f >> 2) & 7);
+                float *blk = reinterpret_cast<float *>(st + ((d >> 6) ? ST_DK : ST_DQ)) +
+                             dablk(i, i) * 256 + f;
+                if (r0 + n >= ulen) *reinterpret_cast<float4 *>(blk) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            {
+                const int n = d >> 3;  // row n of the block, 32-byte part d & 7
+                if (r0 + n >= ulen) {
+                    uint4 *p = reinterpret_cast<uint4 *>(st + ST_Q + (r0 + n) * KD * 2 + (d & 7) * 32);
+                    p[0] = make_uint4(0u, 0u, 0u, 0u);
+                    p[1] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            tc::fence_proxy_async_smem();  // generic writes into a stage TMA refills later
+            tc::named_bar_sync(9 + i, 128);
+        }
+
+        // VARLEN: thread 0 looks up the row range of the unit after next in three
+        // steps spread over this unit (chunk-table entry, then the sequence's bounds,
+        // then the range), all through cp.async into shared memory, so no warp ever
+        // waits on a dependent global load; the refill reads the result.
+        int *vpipe = reinterpret_cast<int *>(smem + SM_VPIPE);
+        int *pend = reinterpret_cast<int *>(smem + SM_PEND) + 2 * sidx;
+        const bool vlead = VARLEN && tid == 0 && u + 2 * stride < units;
+        if (vlead) {
+            const size_t c = (size_t)((unsigned)(u + 2 * stride) / (unsigned)H);
+            cp_async4(vpipe, ex.chunk_indices + 2 * c);
+            cp_async4(vpipe + 1, ex.chunk_indices + 2 * c + 1);
+            cp_async_commit();
+        }
 
         // ---- column-side B operands: dA blocks (j, 0..j-1) transposed.  The loads go
         // out first so their latency overlaps the column loads and the prescale. ----
@@ -327,17 +383,23 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
 #pragma unroll
         for (int m = 0; m < BC / 2; ++m) {
             const int ra = r0 + 2 * m, rb = ra + 1;
-            g2[m] = make_float2(sg[grow_g(ra) * KD + d], sg[grow_g(rb) * KD + d]);
+            g2[m] = make_float2(sg[ra * KD + d], sg[rb * KD + d]);
             k2[m] = make_float2(to_f32(sk[ra * KD + d]), to_f32(sk[rb * KD + d]));
-            if (VARLEN && ra >= ulen) k2[m].x = 0.f;
-            if (VARLEN && rb >= ulen) k2[m].y = 0.f;
+        }
+        if (partial) {
+#pragma unroll
+            for (int m = 0; m < BC / 2; ++m) {
+                const int ra = r0 + 2 * m, rb = ra + 1;
+                if (ra >= ulen) g2[m].x = glastv, k2[m].x = 0.f;
+                if (rb >= ulen) g2[m].y = glastv, k2[m].y = 0.f;
+            }
         }
 #define KDA_EL(arr, r) (((r) & 1) ? arr[(r) >> 1].y : arr[(r) >> 1].x)
 
         // ---- prescaled TF32 operands and post-factors into TMEM ----
         float c2 = 0.f, c3 = 0.f;  // 2^(g_16(i+2) - g_e(i)), 2^(g_16(i+3) - g_e(i))
         if (i < NBLK - 1) {
-            const float ge = sg[grow_g(r0 + BC) * KD + d];
+            const float ge = gsel(r0 + BC, sg[(r0 + BC) * KD + d]);
             float a[BC], v[BC];
 #pragma unroll
             for (int s = 0; s < BC; ++s) {
@@ -347,13 +409,13 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             tc::tmem_st16(tlane + TM_FA + 16 * i, a);
             tc::tmem_st16(tlane + tm_arow(i + 1) + 16 * i, v);
             if (i + 2 < NBLK) {
-                c2 = ex2(sg[grow_g(r0 + 2 * BC) * KD + d] - ge);
+                c2 = ex2(gsel(r0 + 2 * BC, sg[(r0 + 2 * BC) * KD + d]) - ge);
 #pragma unroll
                 for (int s = 0; s < BC; ++s) a[s] = v[s] * c2;
                 tc::tmem_st16(tlane + tm_arow(i + 2) + 16 * i, a);
             }
             if (i + 3 < NBLK) {
-                c3 = ex2(sg[grow_g(r0 + 3 * BC) * KD + d] - ge);
+                c3 = ex2(gsel(r0 + 3 * BC, sg[(r0 + 3 * BC) * KD + d]) - ge);
 #pragma unroll
                 for (int s = 0; s < BC; ++s) a[s] = v[s] * c3;
                 tc::tmem_st16(tlane + tm_arow(i + 3) + 16 * i, a);
@@ -366,8 +428,7 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             for (int r = 1; r < BC; ++r) b[r] = ex2(KDA_EL(g2, r) - g2[0].x);
             tc::tmem_st16(tlane + TM_FB + 16 * (i - 1), b);
 #pragma unroll
-            for (int r = 0; r < BC; ++r)
-                v[r] = (VARLEN && r0 + r >= ulen) ? 0.f : to_f32(sq[(r0 + r) * KD + d]) * b[r];
+            for (int r = 0; r < BC; ++r) v[r] = to_f32(sq[(r0 + r) * KD + d]) * b[r];
             tc::tmem_st16(tlane + TM_AQB + 16 * (i - 1), v);
 #pragma unroll
             for (int r = 0; r < BC; ++r) v[r] = sbeta[r0 + r] * KDA_EL(k2, r) * b[r];
@@ -429,6 +490,16 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             }
         }
         __syncwarp();
+        if (vlead) {  // lookup step 2: the sequence's bounds (an entry naming no sequence
+                      // is marked with chunk -1 and reads nothing)
+            cp_async_wait_all();
+            const int n = vpipe[0], j = vpipe[1];
+            const bool named = n >= 0 && n < ex.num_seqs && j >= 0;
+            if (!named) vpipe[1] = -1;
+            cp_async4_zfill(vpipe + 2, named ? ex.cu_seqlens + n : ex.cu_seqlens, named);
+            cp_async4_zfill(vpipe + 3, named ? ex.cu_seqlens + n + 1 : ex.cu_seqlens, named);
+            cp_async_commit();
+        }
 
         // ---- diagonal block: one exp2 per (r, s, d), shared by both sides, two source
         // rows at a time in packed FP32x2.  Rows run in descending order: once row r is
@@ -450,7 +521,6 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             orow0 = grow(un, r0, T, H);
         }
         const size_t obase = orow0 * KD + d;
-        static_assert(KD == 128, "the db row below recovers orow0 as obase >> 7");
         const uint32_t hk = (uint32_t)H * KD;
 
         auto diag_row = [&](const int r) {
@@ -497,12 +567,12 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         // incoming gradients (ACCUM): fetched three output rows ahead of their use
         float inq[BC], ink[BC], ing[BC];
         auto fetch_in = [&](const int r) {
-            if (VARLEN && r0 + r >= ulen) return;
             if constexpr (ACCUM) {
+                const bool live = !VARLEN || r0 + r < ulen;
                 const size_t off = obase + (size_t)((uint32_t)r * hk);
-                inq[r] = ex.dq_in ? __ldg(ex.dq_in + off) : 0.f;
-                ink[r] = ex.dk_in ? __ldg(ex.dk_in + off) : 0.f;
-                ing[r] = ex.dg_in ? __ldg(ex.dg_in + off) : 0.f;
+                inq[r] = (live && ex.dq_in) ? __ldg(ex.dq_in + off) : 0.f;
+                ink[r] = (live && ex.dk_in) ? __ldg(ex.dk_in + off) : 0.f;
+                ing[r] = (live && ex.dg_in) ? __ldg(ex.dg_in + off) : 0.f;
             }
         };
         float fold_run = 0.f;  // FOLD: running suffix sum of dg inside the sub-block
@@ -511,33 +581,35 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             const int row = r0 + r;
             const size_t off = obase + (size_t)((uint32_t)r * hk);
             if (r >= 3) fetch_in(r - 3);
-            if (VARLEN && row >= ulen) {
-                dbv[r] = 0.f;
-                return;
-            }
+            const bool live = !VARLEN || row < ulen;  // foreign rows: nothing is stored
             const float qv = to_f32(sq[row * KD + d]);
             const float kv = KDA_EL(k2, r), dkv = KDA_EL(dkt2, r);
-            const float pk = sbeta[row] * acck[r];
-            float vq = accq[r], vk = pk + dkv, vg = LN2 * fmaf(qv, accq[r], (pk - dkv) * kv);
+            // every rounding spelled out (no compiler-chosen contraction), so all
+            // instantiations give bitwise the same values
+            const float pk = __fmul_rn(sbeta[row], acck[r]);
+            float vq = accq[r], vk = fmaf(sbeta[row], acck[r], dkv);
+            float vg = __fmul_rn(LN2, fmaf(qv, accq[r], __fmul_rn(__fsub_rn(pk, dkv), kv)));
             if constexpr (ACCUM) {
                 vq += inq[r];
                 vk += ink[r];
                 vg += ing[r];
             }
-            if constexpr (EMIT) {
-                reinterpret_cast<io_t *>(dq_out)[off] = from_f32<io_t>(vq);
-                reinterpret_cast<io_t *>(dk_out)[off] = from_f32<io_t>(vk);
-            } else {
-                dq[off] = vq;
-                dk[off] = vk;
+            if (live) {
+                if constexpr (EMIT) {
+                    reinterpret_cast<io_t *>(dq_out)[off] = from_f32<io_t>(vq);
+                    reinterpret_cast<io_t *>(dk_out)[off] = from_f32<io_t>(vk);
+                } else {
+                    dq[off] = vq;
+                    dk[off] = vk;
+                }
             }
             if constexpr (FOLD) {
-                fold_run += vg;
+                fold_run += live ? vg : 0.f;
                 bank[row * KD + d] = fold_run;
             } else {
-                dg[off] = vg;
+                if (live) dg[off] = vg;
             }
-            dbv[r] = acck[r] * kv;
+            dbv[r] = acck[r] * kv;  // kv = 0 on foreign rows; their db is never stored
         };
         // db[r] = sum over d of 8 rows at a time: transpose-reduce across the warp's lanes
         // (lane l ends with row (l>>2)&7), then a fixed-order sum over the block's 4 warps.
@@ -566,12 +638,28 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
 #pragma unroll
         for (int r = BC - 1; r >= BC / 2; --r) {
             accq[r] = acck[r] = 0.f;
-            if (!VARLEN || r0 + r < ulen) diag_row(r);
+            diag_row(r);
         }
 
         // ---- cross terms: wait for the MMAs, apply the post-factors ----
         ok &= tc::mbar_wait(mbar, (uint32_t)it & 1u, SPIN_LIMIT);
         tc::fence_after_sync();
+        if (vlead) {  // lookup step 3: the row range, published by warp 0's unit-done
+                      // arrival below
+            cp_async_wait_all();
+            const long long bos = vpipe[2], eos = vpipe[3];
+            const int j = vpipe[1];
+            int start = 0, len = 0;
+            if (j >= 0) {
+                const long long st0 = bos + (long long)BT * j;
+                if (bos >= 0 && st0 < eos && eos <= T) {
+                    start = (int)st0;
+                    len = (int)(eos - st0 < BT ? eos - st0 : BT);
+                }
+            }
+            pend[0] = start;
+            pend[1] = len;
+        }
         if (i > 0) {
             float f[BC], x[BC];
             tc::tmem_ld16(tlane + TM_FB + 16 * (i - 1), f);
@@ -624,7 +712,7 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         db_rows(BC / 2);
 #pragma unroll
         for (int r = BC / 2 - 1; r >= 0; --r) {
-            if (!VARLEN || r0 + r < ulen) diag_row(r);
+            diag_row(r);
             out_row(r);
         }
         db_rows(0);
@@ -632,7 +720,10 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         tc::named_bar_sync(1 + i, 128);
         if ((warp & 3) == 0 && lane < BC && (!VARLEN || r0 + lane < ulen)) {
             const int row = r0 + lane;
-            const size_t brow = ((obase - (size_t)d) >> 7) + (size_t)((uint32_t)lane * (uint32_t)H);
+            // recomputed here rather than kept live across the unit (register budget)
+            const size_t brow =
+                VARLEN ? (size_t)(meta[2 * sidx] + row) * H + (int)((unsigned)u % (unsigned)H)
+                       : grow(decode_unit(u, H, NT), row, T, H);
             float v = (sdbp[row] + sdbp[BT + row]) + (sdbp[2 * BT + row] + sdbp[3 * BT + row]);
             if constexpr (ACCUM) {
                 if (ex.db_in) v += ex.db_in[brow];
@@ -665,7 +756,7 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         if ((prev % TC_WARPS) == TC_WARPS - 1 && u + 2 * stride < units) {
             tc::fence_proxy_async_smem();
             load_unit<VARLEN>(st, &full[sidx], meta + 2 * sidx, tm, beta, u + 2 * stride, T, H,
-                              ex, lane);
+                              ex, lane, pend);
         }
     }
 

@@ -24,6 +24,18 @@ struct BwdArgs {
     int num_seqs = 0, num_chunks = 0;
 };
 
+// Forward: the score matrices Aqk, Akk ([B,T,H,64] fp32, zeros outside the support).
+struct FwdArgs {
+    const void *q, *k;
+    const float *g, *beta;
+    float *Aqk, *Akk;
+    int B, T, H;
+    bool fp16;
+};
+
+// Tensor-core (tcgen05 TF32) forward kernel.
+cudaError_t launch_intra_fwd(const FwdArgs &a, cudaStream_t stream);
+
 // All-FP32 SIMT kernel (one CTA per unit).
 cudaError_t launch_intra_fp32(const BwdArgs &a, cudaStream_t stream);
 

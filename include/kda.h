@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 3
+#define KDA_ABI_VERSION 4
 #define KDA_BT 64  /* chunk length */
 #define KDA_BC 16  /* sub-block length inside a chunk */
 #define KDA_K 128  /* head dimension */
@@ -184,6 +184,26 @@ kda_status_t kda_intra_bwd_ex(const void *q, const void *k, const float *g,
                               void *dq, void *dk, float *db, float *dg,
                               int B, int T, int H, kda_dtype_t qk_dtype,
                               const kda_intra_bwd_opts_t *opts, kda_stream_t stream);
+
+/*
+ * The intra-chunk forward: the two score matrices whose gradients kda_intra_bwd
+ * takes, for every unit (b, h, 64-token chunk) and rows r, s of the chunk,
+ *
+ *   Aqk[r,s] = sum_d q[r,d] k[s,d] E[r,s,d]             (s <= r, else 0)
+ *   Akk[r,s] = beta[r] * sum_d k[r,d] k[s,d] E[r,s,d]   (s <  r, else 0)
+ *
+ * (same definitions as above).  q, k, g, beta as for kda_intra_bwd; Aqk and Akk are
+ * [B, T, H, 64] fp32 device outputs, fully overwritten (zeros outside the support),
+ * 16-byte aligned, not overlapping anything else.  Cross-sub-block entries come from
+ * TF32 tensor-core products through the boundary factorization (every exp2 argument
+ * <= 0), the diagonal 16x16 blocks from FP32 with one exp2 per (r, s, d).
+ * Accuracy: max|err| / max|ref| <= 2e-3 per output tensor.  Same shape rules, status
+ * codes and asynchrony as kda_intra_bwd.
+ */
+kda_status_t kda_intra_fwd(const void *q, const void *k, const float *g,
+                           const float *beta, float *Aqk, float *Akk,
+                           int B, int T, int H, kda_dtype_t qk_dtype,
+                           kda_stream_t stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *kda_status_str(kda_status_t status);

@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for want in ("kda_intra_bwd", "kda_intra_bwd_fp32", "kda_intra_bwd_host",
                  "kda_intra_bwd_host_workspace_bytes", "kda_status_str",
-                 "kda_abi_version", "kda_intra_bwd_ex"):
+                 "kda_abi_version", "kda_intra_bwd_ex", "kda_intra_fwd"):
         assert want in names
 
 
@@ -228,3 +228,40 @@ def test_prepare_chunk_indices():
         kda.prepare_chunk_indices(torch.tensor([1, 5]))
     with pytest.raises(ValueError):
         kda.prepare_chunk_indices(torch.tensor([0, 5, 3]))
+
+
+# ---------------------------------------------------------------- kda_intra_fwd
+
+def fwd_call(lib, B=1, T=64, H=1, dtype=0, **override):
+    ptrs = {n: BASE + i * SPAN for i, n in enumerate(("q", "k", "g", "beta", "Aqk", "Akk"))}
+    ptrs.update(override)
+    vp = ctypes.c_void_p
+    args = [vp(ptrs[n]) for n in ("q", "k", "g", "beta", "Aqk", "Akk")]
+    return lib.kda_intra_fwd(*args, B, T, H, dtype, vp(0))
+
+
+@pytest.mark.parametrize("case,want", [
+    (dict(q=0), ERR_NULL),
+    (dict(Akk=0), ERR_NULL),
+    (dict(T=100), ERR_SHAPE),
+    (dict(H=0), ERR_SHAPE),
+    (dict(B=1 << 16, T=1 << 16), ERR_SHAPE),
+    (dict(dtype=5), ERR_DTYPE),
+    (dict(g=BASE + 2 * SPAN + 4), ERR_ALIGN),
+    (dict(Aqk=BASE + 4 * SPAN + 8), ERR_ALIGN),
+    (dict(beta=BASE + 3 * SPAN + 1), ERR_ALIGN),
+    (dict(Aqk=BASE + 2 * SPAN), ERR_OVERLAP),        # output aliases g
+    (dict(Akk=BASE + 4 * SPAN + 256), ERR_OVERLAP),  # Akk inside Aqk
+])
+def test_fwd_rejected_before_launch(lib, case, want):
+    case = dict(case)
+    shape = {k: case.pop(k) for k in ("B", "T", "H", "dtype") if k in case}
+    rc = fwd_call(lib, **shape, **case)
+    assert rc == want, kda.kda_status_str(rc)
+
+
+def test_fwd_valid_call_reaches_the_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("would launch on a real device")
+    assert fwd_call(lib) in (ERR_CUDA, ERR_DEVICE)

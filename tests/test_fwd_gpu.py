@@ -1,0 +1,106 @@
+"""kda_intra_fwd (the score matrices Aqk, Akk) against the oracle's forward, through
+the C ABI."""
+
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_intra_gb300 as kda
+import kda_inputs
+import oracle
+from tests import _gpu
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3  # max|err| / max|ref| per tensor (TF32 cross terms, fp32 diagonal)
+IN = ("q", "k", "g", "beta")
+
+
+def run_fwd(cpu, **kw):
+    dev = _gpu.to_device({n: cpu[n] for n in IN})
+    return kda.kda_intra_fwd(*(dev[n] for n in IN), **kw)
+
+
+def ref_fwd(cpu):
+    return oracle.intra_fwd(*(cpu[n] for n in IN))
+
+
+def rel(a, b):
+    a = a.detach().double().cpu().numpy() if isinstance(a, torch.Tensor) else a
+    return float(np.max(np.abs(a - b)) / np.max(np.abs(b)))
+
+
+def assert_fwd_close(got, ref, what):
+    errs = {n: rel(a, b) for n, a, b in zip(("Aqk", "Akk"), got, ref)}
+    assert all(e <= TOL for e in errs.values()), f"{what}: {errs}"
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2])
+def test_full_workloads(idx):
+    cpu = kda_inputs.make_config_inputs(idx)
+    assert_fwd_close(run_fwd(cpu), ref_fwd(cpu), kda_inputs.CONFIGS[idx].name)
+
+
+@pytest.mark.parametrize("idx", [3, 4])
+def test_large_workloads_sampled_units(idx):
+    cfg = kda_inputs.CONFIGS[idx]
+    cpu = kda_inputs.make_config_inputs(idx)
+    got = run_fwd(cpu)
+    units = kda_inputs.sample_units(cfg, 24)
+    sub = kda_inputs.gather_units({n: cpu[n] for n in IN}, units, cfg.H, cfg.T)
+    ref = oracle.intra_fwd(*(sub[n] for n in IN))
+    assert_fwd_close(_gpu.gather_outputs(list(got), units), ref, f"{cfg.name} (sampled)")
+    for x in got:
+        assert bool(torch.isfinite(x).all())
+
+
+def test_outputs_fully_written_and_zero_outside_support():
+    cpu = kda_inputs.make_inputs(2, 192, 3, seed=80)
+    dev = _gpu.to_device({n: cpu[n] for n in IN})
+    Aqk = torch.full((2, 192, 3, 64), float("nan"), device="cuda")
+    Akk = torch.full((2, 192, 3, 64), float("nan"), device="cuda")
+    kda.kda_intra_fwd(*(dev[n] for n in IN), Aqk=Aqk, Akk=Akk)
+    assert bool(torch.isfinite(Aqk).all()) and bool(torch.isfinite(Akk).all())
+    lower, strict = kda_inputs.chunk_masks()
+    a = Aqk.view(2, 3, 64, 3, 64).cpu()
+    b = Akk.view(2, 3, 64, 3, 64).cpu()
+    up = ~lower  # s > r
+    for r in range(64):
+        assert bool((a[:, :, r, :, up[r]] == 0).all()), r
+        assert bool((b[:, :, r, :, ~strict[r]] == 0).all()), r
+    assert_fwd_close((Aqk, Akk), ref_fwd(cpu), "small")
+
+
+def test_fp16_gate_stress_small():
+    cpu = kda_inputs.make_inputs(1, 512, 2, gate_lo=-8.0, qk_dtype=torch.float16, seed=81)
+    assert_fwd_close(run_fwd(cpu), ref_fwd(cpu), "fp16 stress")
+
+
+def test_deterministic_and_side_stream():
+    cpu = kda_inputs.make_inputs(2, 256, 4, seed=82)
+    a = run_fwd(cpu)
+    s = torch.cuda.Stream()
+    dev = _gpu.to_device({n: cpu[n] for n in IN})
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        b = kda.kda_intra_fwd(*(dev[n] for n in IN), stream=s)
+    s.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_forward_and_backward_satisfy_euler_identities():
+    """At full size (the headline workload), the two kernels against each other:
+    sum q*dq = sum dAqk*Aqk and sum beta*db = sum dAkk*Akk (homogeneity of Aqk in q
+    and of Akk in beta)."""
+    cpu = kda_inputs.make_config_inputs(2)
+    dev = _gpu.to_device(cpu)
+    Aqk, Akk = kda.kda_intra_fwd(*(dev[n] for n in IN))
+    dq, dk, db, dg = kda.kda_intra_bwd(*(dev[n] for n in _gpu.ARGS))
+    lhs1 = (dev["q"].double() * dq.double()).sum().item()
+    rhs1 = (dev["dAqk"].double() * Aqk.double()).sum().item()
+    lhs2 = (dev["beta"].double() * db.double()).sum().item()
+    rhs2 = (dev["dAkk"].double() * Akk.double()).sum().item()
+    scale1 = (dev["dAqk"].double().abs() * Aqk.double().abs()).sum().item()
+    scale2 = (dev["dAkk"].double().abs() * Akk.double().abs()).sum().item()
+    assert abs(lhs1 - rhs1) <= 1e-3 * scale1, (lhs1, rhs1)
+    assert abs(lhs2 - rhs2) <= 1e-3 * scale2, (lhs2, rhs2)
