@@ -44,8 +44,10 @@ constexpr int FSTAGE = 65536;
 constexpr int FM_STG = 2 * FSTAGE;              // Aqk, Akk tiles: 2 x 2 swizzled 8 KB boxes
 constexpr int FM_B = FM_STG + 32768;            // B_1, B_2, B_3: [16t][128] tf32, K-major
 constexpr int FM_BETA = FM_B + 49152;           // f32 [2][64]
-constexpr int FM_BAR = FM_BETA + 512;           // full[2], mma
-constexpr int FM_TSLOT = FM_BAR + 24;
+constexpr int FM_DIAG = FM_BETA + 512;          // f32 [3][512]: diagonal sums until the epilogue
+constexpr int FM_BAR = FM_DIAG + 3 * 512 * 4;   // full[2], mma, staging free
+constexpr int FM_CNT = FM_BAR + 32;             // operand counter
+constexpr int FM_TSLOT = FM_CNT + 8;
 constexpr int FM_TOTAL = FM_TSLOT + 8;
 constexpr int FM_ALLOC = FM_TOTAL + 1024;       // slack for aligning the base
 static_assert(FM_STG % 1024 == 0, "swizzled staging needs 1024-byte alignment");
@@ -150,6 +152,8 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + FM_BAR);
     uint64_t *mbar = full + 2;
+    uint64_t *stg_free = full + 3;  // completes once per unit: the last tiles have left
+    uint32_t *ops_count = reinterpret_cast<uint32_t *>(smem + FM_CNT);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + FM_TSLOT);
     unsigned char *stg = smem + FM_STG;
     const long long stride = gridDim.x;
@@ -159,6 +163,8 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
         tc::mbar_init(&full[0], FULL_ARRIVALS);
         tc::mbar_init(&full[1], FULL_ARRIVALS);
         tc::mbar_init(mbar, 1);
+        tc::mbar_init(stg_free, 1);
+        ops_count[0] = 0u;
         tc::prefetch_tmap(&tm.q);
         tc::prefetch_tmap(&tm.k);
         tc::prefetch_tmap(&tm.g);
@@ -193,8 +199,7 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
         ok &= tc::mbar_wait(&full[sidx], (uint32_t)(it >> 1) & 1u, SPIN_LIMIT);
 
         // ---- prescale: thread = (TMEM lane m, 32 channels).  Lane m < 64 holds the q
-        // row m, lane m >= 64 the beta*k row m - 64 (A operand); k rows also build the
-        // B operands of every later target block. ----
+        // row m, lane m >= 64 the beta*k row m - 64 (A operand). ----
         {
             const int Lq = warp & 3, d0 = 32 * (warp >> 2);
             const bool isk = Lq >= 2;
@@ -224,54 +229,58 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
                 }
                 tc::tmem_st16(tl + (uint32_t)(d0 + 16 * h), v);
             }
-            if (isk && t < NBLK - 1) {
-                // B_tt[s = r, d] = k_r 2^(g_e - g_r) 2^(g_16tt - g_e), e = 16(t+1), tt > t
-                const int e = BC * (t + 1);
+        }
+        {
+            // B_tt[s, d] = k_s 2^(g_16tt - g_s) for s < 16tt (exponent <= 0): 96 rows of
+            // 32 four-channel chunks, six per thread; a warp covers consecutive rows of
+            // one chunk, so its loads and stores are bank-conflict free.
 #pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) {
-                    const int ch = d0 + 4 * q4;
-                    const uint2 w = *reinterpret_cast<const uint2 *>(sk + swz<2>(r, ch));
-                    const io_t *kk = reinterpret_cast<const io_t *>(&w);
-                    const float4 gs = *reinterpret_cast<const float4 *>(sg + swz<4>(r, ch));
-                    const float4 ge = *reinterpret_cast<const float4 *>(sg + swz<4>(e, ch));
-                    float4 a = make_float4(to_f32(kk[0]) * ex2(ge.x - gs.x),
-                                           to_f32(kk[1]) * ex2(ge.y - gs.y),
-                                           to_f32(kk[2]) * ex2(ge.z - gs.z),
-                                           to_f32(kk[3]) * ex2(ge.w - gs.w));
-                    const uint32_t nofs = (uint32_t)((r >> 3) * 128 + (r & 7) * 16);
-                    for (int tt = t + 1; tt < NBLK; ++tt) {
-                        float4 o = a;
-                        if (tt > t + 1) {
-                            const float4 gt =
-                                *reinterpret_cast<const float4 *>(sg + swz<4>(BC * tt, ch));
-                            o = make_float4(a.x * ex2(gt.x - ge.x), a.y * ex2(gt.y - ge.y),
-                                            a.z * ex2(gt.z - ge.z), a.w * ex2(gt.w - ge.w));
-                        }
-                        *reinterpret_cast<float4 *>(smem + FM_B + boff(tt) + (ch >> 2) * 256 * tt +
-                                                    nofs) = o;
-                    }
-                }
+            for (int j = 0; j < 6; ++j) {
+                const int item = tid + FW_THREADS * j;
+                const int row = item % 96, ch = 4 * (item / 96);
+                const int tt = row < 16 ? 1 : row < 48 ? 2 : 3;
+                const int sr = row - 8 * tt * (tt - 1);  // source row s
+                const uint2 w = *reinterpret_cast<const uint2 *>(sk + swz<2>(sr, ch));
+                const io_t *kk = reinterpret_cast<const io_t *>(&w);
+                const float4 gs = *reinterpret_cast<const float4 *>(sg + swz<4>(sr, ch));
+                const float4 gt = *reinterpret_cast<const float4 *>(sg + swz<4>(BC * tt, ch));
+                const float4 o = make_float4(to_f32(kk[0]) * ex2(gt.x - gs.x),
+                                             to_f32(kk[1]) * ex2(gt.y - gs.y),
+                                             to_f32(kk[2]) * ex2(gt.z - gs.z),
+                                             to_f32(kk[3]) * ex2(gt.w - gs.w));
+                *reinterpret_cast<float4 *>(smem + FM_B + boff(tt) + (ch >> 2) * 256 * tt +
+                                            (sr >> 3) * 128 + (sr & 7) * 16) = o;
             }
         }
+        // operands complete; the last warp to get here issues the 48 MMAs.  Thread 0
+        // also releases the staging once the previous unit's tiles have left it.
         tc::tmem_wait_st();
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
-        if (tid == 0) tc::bulk_wait_read_all();  // the last unit's tiles have left the staging
-        __syncthreads();
-        tc::fence_after_sync();
-        if (warp == 0) {
-            if (tc::elect_one()) {
+        if (tid == 0) {
+            tc::bulk_wait_read_all();
+            tc::mbar_arrive(stg_free);
+        }
+        __syncwarp();
+        {
+            uint32_t prev = 0;
+            if (lane == 0) prev = tc::atomic_add_acq_rel_smem(ops_count, 1u);
+            prev = __shfl_sync(0xffffffffu, prev, 0);
+            if ((prev % 16u) == 15u) {
+                tc::fence_after_sync();
+                if (tc::elect_one()) {
 #pragma unroll
-                for (int t = 1; t < NBLK; ++t) {
-                    const uint64_t b0 =
-                        tc::smem_desc(tc::smem_u32(smem + FM_B + boff(t)), 256 * t, 128);
-                    const uint32_t id = tc::idesc_tf32(128, 16 * t);
+                    for (int t = 1; t < NBLK; ++t) {
+                        const uint64_t b0 =
+                            tc::smem_desc(tc::smem_u32(smem + FM_B + boff(t)), 256 * t, 128);
+                        const uint32_t id = tc::idesc_tf32(128, 16 * t);
 #pragma unroll
-                    for (int kk = 0; kk < KD / 8; ++kk)
-                        tc::mma_tf32_ts(tbase + tm_d(t), tbase + 8 * kk,
-                                        b0 + (uint64_t)((512 * t * kk) >> 4), id, kk > 0);
+                        for (int kk = 0; kk < KD / 8; ++kk)
+                            tc::mma_tf32_ts(tbase + tm_d(t), tbase + 8 * kk,
+                                            b0 + (uint64_t)((512 * t * kk) >> 4), id, kk > 0);
+                    }
+                    tc::mma_commit(mbar);
                 }
-                tc::mma_commit(mbar);
             }
             __syncwarp();
         }
@@ -279,7 +288,9 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
         // ---- diagonal blocks: thread = (block i, rows {a, 15-a}, channel group c).
         // Row r meets sources s = 16i + s0 .. 16i + s0 + 7 (those with s <= r) in one
         // call; the half-warp's 16 lanes then reduce [Aqk sums, Akk sums] over their
-        // channel groups, and lane c writes entry s0 + (c % 8) of Aqk (c < 8) or Akk. ----
+        // channel groups, and lane c keeps entry s0 + (c % 8) of Aqk (c < 8) or Akk
+        // for the epilogue (in shared memory: registers are the scarce resource). ----
+        float *dval = reinterpret_cast<float *>(smem + FM_DIAG) + tid;
         {
             const int i = warp >> 2;
             const int a = 2 * (warp & 3) + (lane >> 4);
@@ -313,22 +324,32 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
                         v[8 + sl] = pk.x + pk.y;
                     }
                 }
-                float sum = reduce16(v, lane);
-                const int sc = s0 + (c & 7);
-                if (c >= 8) sum *= sbeta[r];
-                if (!ok) sum = nan;
-                if (c < 8 ? sc <= last : sc < last)
-                    *reinterpret_cast<float *>(stg + stg_off(c >> 3, r, BC * i + sc)) = sum;
+                const float sum = reduce16(v, lane);
+                return c >= 8 ? sum * sbeta[r] : sum;
             };
-            diag8(BC * i + BC - 1 - a, 0);
-            diag8(BC * i + BC - 1 - a, 8);
-            diag8(BC * i + a, 0);
+            dval[0] = diag8(BC * i + BC - 1 - a, 0);
+            dval[512] = diag8(BC * i + BC - 1 - a, 8);
+            dval[1024] = diag8(BC * i + a, 0);
         }
 
         // ---- cross blocks: TMEM lane m -> row r of Aqk (m < 64) or Akk (m >= 64),
         // warp (Lq, Dq) takes the 16 source columns 16Dq.. of its lanes' target block ----
         ok &= tc::mbar_wait(mbar, (uint32_t)it & 1u, SPIN_LIMIT);
         tc::fence_after_sync();
+        ok &= tc::mbar_wait(stg_free, (uint32_t)it & 1u, SPIN_LIMIT);
+        {  // the diagonal entries kept above
+            const int i = warp >> 2;
+            const int a = 2 * (warp & 3) + (lane >> 4);
+            const int c = lane & 15;
+#pragma unroll
+            for (int x = 0; x < 3; ++x) {
+                const int r = x < 2 ? BC * i + BC - 1 - a : BC * i + a;
+                const int last = r - BC * i, sc = (x == 1 ? 8 : 0) + (c & 7);
+                if (c < 8 ? sc <= last : sc < last)
+                    *reinterpret_cast<float *>(stg + stg_off(c >> 3, r, BC * i + sc)) =
+                        ok ? dval[512 * x] : nan;
+            }
+        }
         {
             const int Lq = warp & 3, Dq = warp >> 2;
             const int r = 32 * (Lq & 1) + lane, tensor = Lq >> 1;
