@@ -301,26 +301,93 @@ kda_status_t kda_intra_bwd_host(const void *q, const void *k, const float *g,
     char *beta_d = w;               w += align256(nrow);
     char *aqk_d = w;                w += align256(nda);
     char *akk_d = w;
-    cudaStream_t s = (cudaStream_t)stream;
+
+    // Pipeline over pieces: contiguous runs of 64-token chunks of the flattened
+    // [1, B*T] token axis (chunks never straddle a sequence since T % 64 == 0).  Inputs
+    // of piece p+1 go up on one internal stream while piece p computes on the caller's
+    // stream and piece p-1 comes down on another, so both copy directions and the
+    // kernel overlap.  Events order everything after earlier work on the caller's
+    // stream, and the caller's stream waits for the last copy.
+    const long long chunks = (long long)B * T / KDA_BT;
+    const size_t in_bytes = 2 * nqk + nk4 + nrow + 2 * nda;
+    long long P = (long long)(in_bytes / ((size_t)32 << 20));
+    if (P < 1) P = 1;
+    if (P > 64) P = 64;
+    if (P > chunks) P = chunks;
+    cudaStream_t s = (cudaStream_t)stream, s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev[2 * 64 + 2] = {};
+    const int nev = (int)(2 * P + 2);
+    kda_status_t result = KDA_OK;
+    auto fail = [&](kda_status_t code) {
+        if (result == KDA_OK) result = code;
+    };
+    if (cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking) != cudaSuccess)
+        fail(KDA_ERR_CUDA);
+    for (int e = 0; e < nev && result == KDA_OK; ++e)
+        if (cudaEventCreateWithFlags(&ev[e], cudaEventDisableTiming) != cudaSuccess)
+            fail(KDA_ERR_CUDA);
     const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
-    if (cudaMemcpyAsync(q_d, q, nqk, h2d, s) != cudaSuccess ||
-        cudaMemcpyAsync(k_d, k, nqk, h2d, s) != cudaSuccess ||
-        cudaMemcpyAsync(g_d, g, nk4, h2d, s) != cudaSuccess ||
-        cudaMemcpyAsync(beta_d, beta, nrow, h2d, s) != cudaSuccess ||
-        cudaMemcpyAsync(aqk_d, dAqk, nda, h2d, s) != cudaSuccess ||
-        cudaMemcpyAsync(akk_d, dAkk, nda, h2d, s) != cudaSuccess)
-        return KDA_ERR_CUDA;
-    st = kda_intra_bwd(q_d, k_d, (const float *)g_d, (const float *)beta_d,
-                       (const float *)aqk_d, (const float *)akk_d, (float *)dq_d,
-                       (float *)dk_d, (float *)db_d, (float *)dg_d, B, T, H, qk_dtype,
-                       stream);
-    if (st != KDA_OK) return st;
-    if (cudaMemcpyAsync(dq, dq_d, nk4, d2h, s) != cudaSuccess ||
-        cudaMemcpyAsync(dk, dk_d, nk4, d2h, s) != cudaSuccess ||
-        cudaMemcpyAsync(dg, dg_d, nk4, d2h, s) != cudaSuccess ||
-        cudaMemcpyAsync(db, db_d, nrow, d2h, s) != cudaSuccess)
-        return KDA_ERR_CUDA;
-    return KDA_OK;
+    if (result == KDA_OK) {
+        cudaEvent_t e_start = ev[0], e_done = ev[1];
+        if (cudaEventRecord(e_start, s) != cudaSuccess ||
+            cudaStreamWaitEvent(s_in, e_start, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(s_out, e_start, 0) != cudaSuccess)
+            fail(KDA_ERR_CUDA);
+        for (long long p = 0; p < P && result == KDA_OK; ++p) {
+            const long long c0 = p * chunks / P, c1 = (p + 1) * chunks / P;
+            const size_t r0 = (size_t)c0 * KDA_BT * H, nr = (size_t)(c1 - c0) * KDA_BT * H;
+            const int Tp = (int)((c1 - c0) * KDA_BT);
+            cudaEvent_t e_in = ev[2 + 2 * p], e_k = ev[3 + 2 * p];
+            const size_t oqk = r0 * KDA_K * 2, o4 = r0 * KDA_K * 4, orow = r0 * 4,
+                         oda = r0 * KDA_BT * 4;
+            const size_t lqk = nr * KDA_K * 2, l4 = nr * KDA_K * 4, lrow = nr * 4,
+                         lda = nr * KDA_BT * 4;
+            if (cudaMemcpyAsync(q_d + oqk, (const char *)q + oqk, lqk, h2d, s_in) != cudaSuccess ||
+                cudaMemcpyAsync(k_d + oqk, (const char *)k + oqk, lqk, h2d, s_in) != cudaSuccess ||
+                cudaMemcpyAsync(g_d + o4, (const char *)g + o4, l4, h2d, s_in) != cudaSuccess ||
+                cudaMemcpyAsync(beta_d + orow, (const char *)beta + orow, lrow, h2d, s_in) !=
+                    cudaSuccess ||
+                cudaMemcpyAsync(aqk_d + oda, (const char *)dAqk + oda, lda, h2d, s_in) !=
+                    cudaSuccess ||
+                cudaMemcpyAsync(akk_d + oda, (const char *)dAkk + oda, lda, h2d, s_in) !=
+                    cudaSuccess ||
+                cudaEventRecord(e_in, s_in) != cudaSuccess ||
+                cudaStreamWaitEvent(s, e_in, 0) != cudaSuccess) {
+                fail(KDA_ERR_CUDA);
+                break;
+            }
+            const kda_status_t st2 = kda_intra_bwd(
+                q_d + oqk, k_d + oqk, (const float *)(g_d + o4), (const float *)(beta_d + orow),
+                (const float *)(aqk_d + oda), (const float *)(akk_d + oda),
+                (float *)(dq_d + o4), (float *)(dk_d + o4), (float *)(db_d + orow),
+                (float *)(dg_d + o4), 1, Tp, H, qk_dtype, stream);
+            if (st2 != KDA_OK) {
+                fail(st2);
+                break;
+            }
+            if (cudaEventRecord(e_k, s) != cudaSuccess ||
+                cudaStreamWaitEvent(s_out, e_k, 0) != cudaSuccess ||
+                cudaMemcpyAsync((char *)dq + o4, dq_d + o4, l4, d2h, s_out) != cudaSuccess ||
+                cudaMemcpyAsync((char *)dk + o4, dk_d + o4, l4, d2h, s_out) != cudaSuccess ||
+                cudaMemcpyAsync((char *)dg + o4, dg_d + o4, l4, d2h, s_out) != cudaSuccess ||
+                cudaMemcpyAsync((char *)db + orow, db_d + orow, lrow, d2h, s_out) !=
+                    cudaSuccess) {
+                fail(KDA_ERR_CUDA);
+                break;
+            }
+        }
+        // the caller's stream waits for the last copy, also after a failure midway
+        if (cudaEventRecord(e_done, s_out) != cudaSuccess ||
+            cudaStreamWaitEvent(s, e_done, 0) != cudaSuccess)
+            fail(KDA_ERR_CUDA);
+    }
+    // released once their queued work is done; nothing here waits for it
+    for (int e = 0; e < nev; ++e)
+        if (ev[e]) cudaEventDestroy(ev[e]);
+    if (s_in) cudaStreamDestroy(s_in);
+    if (s_out) cudaStreamDestroy(s_out);
+    return result;
 }
 
 const char *kda_status_str(kda_status_t status) {

@@ -110,11 +110,15 @@ kda_status_t kda_intra_bwd_fp32(const void *q, const void *k, const float *g,
 /*
  * End-to-end convenience for callers holding HOST buffers: copies the six inputs
  * into `workspace` (device memory of at least kda_intra_bwd_host_workspace_bytes()
- * bytes, caller-owned, 256-byte aligned), runs kda_intra_bwd on `stream`, and copies
- * the four outputs back into the host buffers.  One cudaMemcpyAsync per tensor; the
- * copies are truly asynchronous only when the host buffers are page-locked.  The
- * call returns once everything is queued: synchronise `stream` before reading the
- * outputs or reusing the inputs.  Host pointers need no particular alignment.
+ * bytes, caller-owned, 256-byte aligned), runs kda_intra_bwd, and copies the four
+ * outputs back into the host buffers.  The work is pipelined over pieces of about
+ * 32 MB of input (whole 64-token chunks): uploads run on one internal stream,
+ * downloads on another and the kernels on `stream`, so both copy directions and the
+ * compute overlap; events order it all after earlier work on `stream`, and `stream`
+ * waits for the last download.  Copies are truly asynchronous only when the host
+ * buffers are page-locked.  The call returns once everything is queued: synchronise
+ * `stream` before reading the outputs or reusing the inputs.  Host pointers need no
+ * particular alignment.
  */
 size_t kda_intra_bwd_host_workspace_bytes(int B, int T, int H, kda_dtype_t qk_dtype);
 

@@ -164,6 +164,25 @@ def test_host_entry_point_matches_device_path():
         assert torch.equal(a, b.cpu()), n
 
 
+@pytest.mark.parametrize("pinned_host", [True, False])
+def test_host_entry_point_pipelined_pieces(pinned_host):
+    """About 100 MB of input: the host entry point splits it into three pieces of
+    42-43 chunks on its internal streams; the result is bitwise the device path's."""
+    B, T, H = 4, 2048, 8
+    cpu = kda_inputs.make_inputs(B, T, H, seed=19)
+    host = {n: (v.pin_memory() if pinned_host else v.clone()) for n, v in cpu.items()}
+    mk = (lambda *shape: torch.empty(*shape).pin_memory()) if pinned_host else torch.empty
+    outs = [mk(B, T, H, 128), mk(B, T, H, 128), mk(B, T, H), mk(B, T, H, 128)]
+    ws = torch.empty(kda.kda_intra_bwd_host_workspace_bytes(B, T, H, torch.bfloat16),
+                     dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    kda.kda_intra_bwd_host(*(host[n] for n in _gpu.ARGS), *outs, workspace=ws, stream=side)
+    side.synchronize()
+    ref = _gpu.run("kda_intra_bwd", _gpu.to_device(cpu))
+    for n, a, b in zip(_gpu.NAMES, outs, ref):
+        assert torch.equal(a, b.cpu()), n
+
+
 def test_misaligned_pointer_is_a_status_not_a_fault():
     cpu = kda_inputs.make_inputs(1, 64, 1, seed=18)
     dev = _gpu.to_device(cpu)
