@@ -70,6 +70,13 @@ def test_outputs_fully_written_and_zero_outside_support():
     assert_fwd_close((Aqk, Akk), ref_fwd(cpu), "small")
 
 
+@pytest.mark.parametrize("B,T,H,dtype", [(1, 64, 1, torch.bfloat16), (3, 128, 5, torch.float16),
+                                         (2, 320, 7, torch.bfloat16), (1, 64, 200, torch.float16)])
+def test_odd_shapes(B, T, H, dtype):
+    cpu = kda_inputs.make_inputs(B, T, H, qk_dtype=dtype, seed=83 + H)
+    assert_fwd_close(run_fwd(cpu), ref_fwd(cpu), f"B={B} T={T} H={H}")
+
+
 def test_fp16_gate_stress_small():
     cpu = kda_inputs.make_inputs(1, 512, 2, gate_lo=-8.0, qk_dtype=torch.float16, seed=81)
     assert_fwd_close(run_fwd(cpu), ref_fwd(cpu), "fp16 stress")
