@@ -44,8 +44,8 @@ constexpr int FSTAGE = 65536;
 constexpr int FM_STG = 2 * FSTAGE;              // Aqk, Akk tiles: 2 x 2 swizzled 8 KB boxes
 constexpr int FM_B = FM_STG + 32768;            // B_1, B_2, B_3: [16t][128] tf32, K-major
 constexpr int FM_BETA = FM_B + 49152;           // f32 [2][64]
-constexpr int FM_DIAG = FM_BETA + 512;          // f32 [3][512]: diagonal sums until the epilogue
-constexpr int FM_BAR = FM_DIAG + 3 * 512 * 4;   // full[2], mma, staging free
+constexpr int FM_DIAG = FM_BETA + 512;          // f32 [2][512]: diagonal sums until the epilogue
+constexpr int FM_BAR = FM_DIAG + 2 * 512 * 4;   // full[2], mma, staging free
 constexpr int FM_CNT = FM_BAR + 32;             // operand counter
 constexpr int FM_TSLOT = FM_CNT + 8;
 constexpr int FM_TOTAL = FM_TSLOT + 8;
@@ -285,51 +285,81 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
             __syncwarp();
         }
 
-        // ---- diagonal blocks: thread = (block i, rows {a, 15-a}, channel group c).
-        // Row r meets sources s = 16i + s0 .. 16i + s0 + 7 (those with s <= r) in one
-        // call; the half-warp's 16 lanes then reduce [Aqk sums, Akk sums] over their
-        // channel groups, and lane c keeps entry s0 + (c % 8) of Aqk (c < 8) or Akk
-        // for the epilogue (in shared memory: registers are the scarce resource). ----
+        // ---- diagonal blocks: thread = (block i, rows rb = 16i+15-a and ra = 16i+a,
+        // channel group c).  Two 16-slot transposed reductions over the half-warp's 16
+        // channel groups: the first holds rb against sources 16i..16i+7 (Aqk, Akk),
+        // the second packs rb against 16i+8..rb and ra against 16i..ra into the 16
+        // slots exactly (7-a + a+1 Aqk, 7-a + a Akk, and rb's own Aqk diagonal in the
+        // one Akk slot left free).  Lane c keeps slot c for the epilogue. ----
         float *dval = reinterpret_cast<float *>(smem + FM_DIAG) + tid;
         {
             const int i = warp >> 2;
             const int a = 2 * (warp & 3) + (lane >> 4);
             const int c = lane & 15;
+            const int rb = BC * i + BC - 1 - a, ra = BC * i + a;
             const float2 neg1 = make_float2(-1.f, -1.f);
-            auto diag8 = [&](const int r, const int s0) {
-                const int last = r - BC * i;  // in-block index of the diagonal source
+            // sums over this lane's 8 channels of q_r k_s E and k_r k_s E
+            auto src = [&](const float2(&qv)[4], const float2(&kv)[4], const float2(&gv)[4],
+                           const int srow, float &oq, float &ok_) {
+                float2 ks[4], gs[4];
+                ld8_io<io_t>(sk, srow, c, ks);
+                ld8_f32(sg, srow, c, gs);
+                float2 pq = make_float2(0.f, 0.f), pk = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const float2 df = __ffma2_rn(gs[x], neg1, gv[x]);
+                    const float2 tq = __fmul2_rn(ks[x], make_float2(ex2(df.x), ex2(df.y)));
+                    pq = __ffma2_rn(qv[x], tq, pq);
+                    pk = __ffma2_rn(kv[x], tq, pk);
+                }
+                oq = pq.x + pq.y;
+                ok_ = pk.x + pk.y;
+            };
+            float v[16];
+            {
                 float2 qv[4], kv[4], gv[4];
-                ld8_io<io_t>(sq, r, c, qv);
-                ld8_io<io_t>(sk, r, c, kv);
-                ld8_f32(sg, r, c, gv);
-                float v[16];
+                ld8_io<io_t>(sq, rb, c, qv);
+                ld8_io<io_t>(sk, rb, c, kv);
+                ld8_f32(sg, rb, c, gv);
 #pragma unroll
-                for (int sl = 0; sl < 8; ++sl) {
-                    v[sl] = v[8 + sl] = 0.f;
-                    // keep the loads of at most two sources in flight (register budget)
-                    if ((sl & 1) == 0) asm volatile("" ::: "memory");
-                    if (s0 + sl <= last) {
-                        float2 ks[4], gs[4];
-                        ld8_io<io_t>(sk, BC * i + s0 + sl, c, ks);
-                        ld8_f32(sg, BC * i + s0 + sl, c, gs);
-                        float2 pq = make_float2(0.f, 0.f), pk = make_float2(0.f, 0.f);
+                for (int j = 0; j < 8; ++j) {
+                    if ((j & 1) == 0) asm volatile("" ::: "memory");
+                    src(qv, kv, gv, BC * i + j, v[j], v[8 + j]);
+                }
+                dval[0] = reduce16(v, lane);
 #pragma unroll
-                        for (int x = 0; x < 4; ++x) {
-                            const float2 df = __ffma2_rn(gs[x], neg1, gv[x]);
-                            const float2 tq = __fmul2_rn(ks[x], make_float2(ex2(df.x), ex2(df.y)));
-                            pq = __ffma2_rn(qv[x], tq, pq);
-                            pk = __ffma2_rn(kv[x], tq, pk);
+                for (int j = 0; j < 8; ++j) {
+                    v[j] = v[8 + j] = 0.f;
+                    if ((j & 1) == 0) asm volatile("" ::: "memory");
+                    if (j <= 7 - a) {
+                        float oq, ok_;
+                        src(qv, kv, gv, BC * i + 8 + j, oq, ok_);
+                        if (j == 7 - a) {
+                            v[8 + j] = oq;  // Aqk[rb][rb]
+                        } else {
+                            v[j] = oq;
+                            v[8 + j] = ok_;
                         }
-                        v[sl] = pq.x + pq.y;
-                        v[8 + sl] = pk.x + pk.y;
                     }
                 }
-                const float sum = reduce16(v, lane);
-                return c >= 8 ? sum * sbeta[r] : sum;
-            };
-            dval[0] = diag8(BC * i + BC - 1 - a, 0);
-            dval[512] = diag8(BC * i + BC - 1 - a, 8);
-            dval[1024] = diag8(BC * i + a, 0);
+            }
+            {
+                float2 qv[4], kv[4], gv[4];
+                ld8_io<io_t>(sq, ra, c, qv);
+                ld8_io<io_t>(sk, ra, c, kv);
+                ld8_f32(sg, ra, c, gv);
+#pragma unroll
+                for (int sl = 0; sl < 8; ++sl) {
+                    if ((sl & 1) == 0) asm volatile("" ::: "memory");
+                    if (sl <= a) {
+                        float oq, ok_;
+                        src(qv, kv, gv, BC * i + sl, oq, ok_);
+                        v[7 - sl] = oq;
+                        if (sl < a) v[15 - sl] = ok_;
+                    }
+                }
+            }
+            dval[512] = reduce16(v, lane);
         }
 
         // ---- cross blocks: TMEM lane m -> row r of Aqk (m < 64) or Akk (m >= 64),
@@ -341,13 +371,30 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
             const int i = warp >> 2;
             const int a = 2 * (warp & 3) + (lane >> 4);
             const int c = lane & 15;
-#pragma unroll
-            for (int x = 0; x < 3; ++x) {
-                const int r = x < 2 ? BC * i + BC - 1 - a : BC * i + a;
-                const int last = r - BC * i, sc = (x == 1 ? 8 : 0) + (c & 7);
-                if (c < 8 ? sc <= last : sc < last)
-                    *reinterpret_cast<float *>(stg + stg_off(c >> 3, r, BC * i + sc)) =
-                        ok ? dval[512 * x] : nan;
+            const int rb = BC * i + BC - 1 - a, ra = BC * i + a;
+            // first reduction: Aqk[rb][16i + c] (c < 8), Akk[rb][16i + c - 8]
+            {
+                const float val = c < 8 ? dval[0] : dval[0] * sbeta[rb];
+                *reinterpret_cast<float *>(stg + stg_off(c >> 3, rb, BC * i + (c & 7))) =
+                    ok ? val : nan;
+            }
+            // second reduction: the packed slots
+            {
+                int tensor, r, col;
+                float scale = 1.f;
+                if (c <= 6 - a) {
+                    tensor = 0, r = rb, col = 8 + c;
+                } else if (c <= 7) {
+                    tensor = 0, r = ra, col = 7 - c;
+                } else if (c <= 14 - a) {
+                    tensor = 1, r = rb, col = c, scale = sbeta[rb];
+                } else if (c == 15 - a) {
+                    tensor = 0, r = rb, col = 15 - a;
+                } else {
+                    tensor = 1, r = ra, col = 15 - c, scale = sbeta[ra];
+                }
+                *reinterpret_cast<float *>(stg + stg_off(tensor, r, BC * i + col)) =
+                    ok ? dval[512] * scale : nan;
             }
         }
         {
