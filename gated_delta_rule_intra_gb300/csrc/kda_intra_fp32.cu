@@ -108,16 +108,22 @@ kda_intra_bwd_fp32_kernel(const io_t *__restrict__ q, const io_t *__restrict__ k
 #pragma unroll
     for (int r = 0; r < BC; ++r) accq[r] = acck[r] = dkt[r] = 0.f;
 
-    // ---- row side: target block i, source blocks j < i ----
+    // ---- row side: target block i, source blocks j < i; four source columns per
+    // 16-byte load of each dA row ----
     for (int j = 0; j < i; ++j) {
         const float cj = (j == i - 1) ? 1.f : ex2(gr[0] - s.g[BC * (j + 1)][d]);
-        for (int sl = 0; sl < BC; ++sl) {
-            const int sc = BC * j + sl;
-            const float kv = s.kb[sc][d] * cj;
+#pragma unroll 1
+        for (int s4 = 0; s4 < BC; s4 += 4) {
+            const int sc = BC * j + s4;
+            float kv[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) kv[x] = s.kb[sc + x][d] * cj;
 #pragma unroll
             for (int r = 0; r < BC; ++r) {
-                accq[r] = fmaf(s.daqk[r0 + r][sc], kv, accq[r]);
-                acck[r] = fmaf(s.dakk[r0 + r][sc], kv, acck[r]);
+                const float4 aq = *reinterpret_cast<const float4 *>(&s.daqk[r0 + r][sc]);
+                const float4 ak = *reinterpret_cast<const float4 *>(&s.dakk[r0 + r][sc]);
+                accq[r] = fmaf(aq.x, kv[0], fmaf(aq.y, kv[1], fmaf(aq.z, kv[2], fmaf(aq.w, kv[3], accq[r]))));
+                acck[r] = fmaf(ak.x, kv[0], fmaf(ak.y, kv[1], fmaf(ak.z, kv[2], fmaf(ak.w, kv[3], acck[r]))));
             }
         }
     }
@@ -130,16 +136,24 @@ kda_intra_bwd_fp32_kernel(const io_t *__restrict__ q, const io_t *__restrict__ k
         }
     }
 
-    // ---- column side: source block i, target blocks j > i ----
+    // ---- column side: source block i, target blocks j > i; each dA row segment of
+    // the source block read as four 16-byte loads ----
     for (int j = i + 1; j < NBLK; ++j) {
         const float cj = (j == i + 1) ? 1.f : ex2(s.g[BC * j][d] - s.g[r0 + BC][d]);
+#pragma unroll 2
         for (int rl = 0; rl < BC; ++rl) {
             const int rr = BC * j + rl;
             const float qv = s.qb[rr - BC][d] * cj;
             const float kv = s.kbb[rr - BC][d] * cj;
 #pragma unroll
-            for (int sl = 0; sl < BC; ++sl)
-                dkt[sl] = fmaf(s.daqk[rr][r0 + sl], qv, fmaf(s.dakk[rr][r0 + sl], kv, dkt[sl]));
+            for (int s4 = 0; s4 < BC; s4 += 4) {
+                const float4 aq = *reinterpret_cast<const float4 *>(&s.daqk[rr][r0 + s4]);
+                const float4 ak = *reinterpret_cast<const float4 *>(&s.dakk[rr][r0 + s4]);
+                dkt[s4 + 0] = fmaf(aq.x, qv, fmaf(ak.x, kv, dkt[s4 + 0]));
+                dkt[s4 + 1] = fmaf(aq.y, qv, fmaf(ak.y, kv, dkt[s4 + 1]));
+                dkt[s4 + 2] = fmaf(aq.z, qv, fmaf(ak.z, kv, dkt[s4 + 2]));
+                dkt[s4 + 3] = fmaf(aq.w, qv, fmaf(ak.w, kv, dkt[s4 + 3]));
+            }
         }
     }
     if (i < NBLK - 1) {
