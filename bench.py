@@ -369,10 +369,20 @@ def run_ours(args, cfg):
         cpu["k"] = cpu["k"][:, :, ::args.gva].contiguous()
     x = {n: v.to(dev) for n, v in cpu.items()}
     ins = [x[n] for n in ("q", "k", "g", "beta", "dAqk", "dAkk")]
+    fwd = args.path == "kda_intra_fwd"
     extended = (args.gva > 1 or args.accumulate or args.fold_dg or args.io_dtype_out
                 or args.varlen)
     opts = None
-    if extended:
+    if fwd:
+        if args.accumulate or args.fold_dg or args.io_dtype_out:
+            raise SystemExit("the forward takes --gva and --varlen only")
+        outs = list(kda.kda_intra_fwd(*ins[:4], **varlen))
+        if extended:
+            opts = {"value_heads_per_qk_head": args.gva, "varlen": args.varlen}
+
+        def step():
+            kda.kda_intra_fwd(*ins[:4], *outs, **varlen, stream=stream)
+    elif extended:
         gen = torch.Generator().manual_seed(seed + 1)
         extra = dict(varlen)
         if args.accumulate:
@@ -389,11 +399,6 @@ def run_ours(args, cfg):
         def step():
             kda.kda_intra_bwd_ex(*ins, *outs, **extra, fold_dg=args.fold_dg,
                                  dqdk_io_dtype=args.io_dtype_out, stream=stream)
-    elif args.path == "kda_intra_fwd":
-        outs = list(kda.kda_intra_fwd(*ins[:4]))
-
-        def step():
-            kda.kda_intra_fwd(*ins[:4], *outs, stream=stream)
     else:
         fn = getattr(kda, args.path)
         outs = kda._outputs(x["q"], None, None, None, None)
@@ -427,7 +432,6 @@ def run_ours(args, cfg):
 
     # end to end through the host-buffer entry point
     e2e = None
-    fwd = args.path == "kda_intra_fwd"
     if not args.no_e2e and not extended and not fwd:
         pin = {n: v.pin_memory() for n, v in cpu.items()}
         hout = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
@@ -464,14 +468,17 @@ def run_ours(args, cfg):
     if rank != 0:
         return
     qk_bytes = torch.tensor([], dtype=cfg.qk_dtype).element_size()
-    if args.varlen:
+    if fwd:
+        # per valid token row and head: q, k, g, beta in; both 64-column rows out
+        per_row = 2 * kda_inputs.K * qk_bytes / args.gva + kda_inputs.K * 4 + 4 + 2 * 64 * 4
+        rows = cfg.T * cfg.B if args.varlen else cfg.units * kda_inputs.BT / cfg.H
+        bytes_per_launch = rows * cfg.H * per_row
+    elif args.varlen:
         bytes_per_launch = varlen_algorithmic_bytes(cfg.lens, cfg.H, qk_bytes,
                                                     accumulate=args.accumulate,
                                                     io_out=args.io_dtype_out)
         if args.gva > 1:
             bytes_per_launch -= cfg.T * cfg.H * 2 * kda_inputs.K * qk_bytes * (1 - 1 / args.gva)
-    elif fwd:
-        bytes_per_launch = cfg.units * FWD_BYTES_PER_UNIT
     else:
         bytes_per_launch = cfg.units * algorithmic_bytes_per_unit(
             qk_bytes, group=args.gva, accumulate=args.accumulate, io_out=args.io_dtype_out)
@@ -487,7 +494,8 @@ def run_ours(args, cfg):
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32" if args.path.endswith("fp32") else "tf32+f32",
         "data": "synthetic",
-        "config": config_dict(cfg, "kda_intra_bwd_ex" if extended else args.path, opts),
+        "config": config_dict(cfg, args.path if fwd else
+                              "kda_intra_bwd_ex" if extended else args.path, opts),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"

@@ -13,7 +13,8 @@ The functions carry the C names of ``include/kda.h``:
   the q/k dtype, variable-length sequences (``cu_seqlens``)
 * ``prepare_chunk_indices`` -- the (sequence, chunk) table of a ``cu_seqlens``
 * ``kda_intra_bwd_host``  -- host buffers in and out, copies on the stream
-* ``kda_intra_fwd``       -- the forward score matrices Aqk, Akk
+* ``kda_intra_fwd``       -- the forward score matrices Aqk, Akk (grouped value heads
+  and variable-length sequences through ``kda_intra_fwd_ex``)
 * ``kda_status_str``, ``kda_abi_version``
 """
 
@@ -46,6 +47,13 @@ class KdaOpts(ctypes.Structure):
                 ("num_seqs", ctypes.c_int), ("num_chunks", ctypes.c_int)]
 
 
+class KdaFwdOpts(ctypes.Structure):
+    """Mirror of kda_intra_fwd_opts_t."""
+    _fields_ = [("HV", ctypes.c_int), ("cu_seqlens", ctypes.c_void_p),
+                ("chunk_indices", ctypes.c_void_p), ("num_seqs", ctypes.c_int),
+                ("num_chunks", ctypes.c_int)]
+
+
 class KdaError(RuntimeError):
     def __init__(self, code: int, fn: str):
         self.code = code
@@ -75,6 +83,9 @@ def load_library(path: str | None = None):
     lib.kda_intra_bwd_host.restype = st
     lib.kda_intra_fwd.argtypes = [vp, vp, fp, fp, fp, fp, i, i, i, i, vp]
     lib.kda_intra_fwd.restype = st
+    lib.kda_intra_fwd_ex.argtypes = [vp, vp, fp, fp, fp, fp, i, i, i, i,
+                                     ctypes.POINTER(KdaFwdOpts), vp]
+    lib.kda_intra_fwd_ex.restype = st
     lib.kda_intra_bwd_host_workspace_bytes.argtypes = [i, i, i, i]
     lib.kda_intra_bwd_host_workspace_bytes.restype = ctypes.c_size_t
     lib.kda_status_str.argtypes = [i]
@@ -249,17 +260,7 @@ def kda_intra_bwd_ex(q, k, g, beta, dAqk, dAkk, dq=None, dk=None, db=None, dg=No
             setattr(opts, name, t.data_ptr())
     opts.fold_dg = int(bool(fold_dg))
     opts.dqdk_io_dtype = int(bool(dqdk_io_dtype))
-    if cu_seqlens is not None:
-        if chunk_indices is None:
-            chunk_indices = prepare_chunk_indices(cu_seqlens)
-        _check("cu_seqlens", cu_seqlens, (cu_seqlens.numel(),), torch.int32, dev)
-        _check("chunk_indices", chunk_indices, (chunk_indices.shape[0], 2), torch.int32, dev)
-        opts.cu_seqlens = cu_seqlens.data_ptr()
-        opts.chunk_indices = chunk_indices.data_ptr() if chunk_indices.numel() else 0
-        opts.num_seqs = cu_seqlens.numel() - 1
-        opts.num_chunks = chunk_indices.shape[0]
-    elif chunk_indices is not None:
-        raise ValueError("chunk_indices needs cu_seqlens")
+    _varlen_opts(opts, cu_seqlens, chunk_indices, dev)
     lib = load_library()
     ptr = ctypes.c_void_p
     with torch.cuda.device(dev):
@@ -273,31 +274,55 @@ def kda_intra_bwd_ex(q, k, g, beta, dAqk, dAkk, dq=None, dk=None, db=None, dg=No
     return dq, dk, db, dg
 
 
-def kda_intra_fwd(q, k, g, beta, Aqk=None, Akk=None, stream=None):
-    """Aqk, Akk ([B, T, H, 64] fp32, zeros outside the support) of the intra-chunk
-    forward on the CUDA tensors q, k ([B, T, H, 128] bf16/fp16), g ([B, T, H, 128]
-    fp32) and beta ([B, T, H] fp32)."""
+def _varlen_opts(opts, cu_seqlens, chunk_indices, dev):
+    if cu_seqlens is not None:
+        if chunk_indices is None:
+            chunk_indices = prepare_chunk_indices(cu_seqlens)
+        _check("cu_seqlens", cu_seqlens, (cu_seqlens.numel(),), torch.int32, dev)
+        _check("chunk_indices", chunk_indices, (chunk_indices.shape[0], 2), torch.int32, dev)
+        opts.cu_seqlens = cu_seqlens.data_ptr()
+        opts.chunk_indices = chunk_indices.data_ptr() if chunk_indices.numel() else 0
+        opts.num_seqs = cu_seqlens.numel() - 1
+        opts.num_chunks = chunk_indices.shape[0]
+    elif chunk_indices is not None:
+        raise ValueError("chunk_indices needs cu_seqlens")
+
+
+def kda_intra_fwd(q, k, g, beta, Aqk=None, Akk=None, *, cu_seqlens=None, chunk_indices=None,
+                  stream=None):
+    """Aqk, Akk ([B, T, HV, 64] fp32, zeros outside the support) of the intra-chunk
+    forward on the CUDA tensors q, k ([B, T, H, 128] bf16/fp16), g ([B, T, HV, 128]
+    fp32) and beta ([B, T, HV] fp32); HV = g.shape[2] is a multiple of H (value head
+    hv reads q/k head hv // (HV // H)).  ``cu_seqlens`` / ``chunk_indices`` as for
+    ``kda_intra_bwd_ex``."""
     if q.device.type != "cuda":
         raise ValueError("kda_intra_fwd needs CUDA tensors (no CPU path exists)")
     B, T, H = _shape(q)
     if q.dtype not in _DTYPES:
         raise ValueError(f"q/k dtype must be bf16 or fp16, got {q.dtype}")
+    if g.dim() != 4:
+        raise ValueError("g must be [B, T, HV, 128]")
+    HV = g.shape[2]
     dev, f32 = q.device, torch.float32
-    Aqk = torch.empty(B, T, H, BT, device=dev, dtype=f32) if Aqk is None else Aqk
-    Akk = torch.empty(B, T, H, BT, device=dev, dtype=f32) if Akk is None else Akk
+    Aqk = torch.empty(B, T, HV, BT, device=dev, dtype=f32) if Aqk is None else Aqk
+    Akk = torch.empty(B, T, HV, BT, device=dev, dtype=f32) if Akk is None else Akk
     _check("k", k, (B, T, H, K), q.dtype, dev)
-    _check("g", g, (B, T, H, K), f32, dev)
-    _check("beta", beta, (B, T, H), f32, dev)
-    _check("Aqk", Aqk, (B, T, H, BT), f32, dev)
-    _check("Akk", Akk, (B, T, H, BT), f32, dev)
+    _check("g", g, (B, T, HV, K), f32, dev)
+    _check("beta", beta, (B, T, HV), f32, dev)
+    _check("Aqk", Aqk, (B, T, HV, BT), f32, dev)
+    _check("Akk", Akk, (B, T, HV, BT), f32, dev)
+    opts = KdaFwdOpts()
+    opts.HV = HV
+    _varlen_opts(opts, cu_seqlens, chunk_indices, dev)
     lib = load_library()
     ptr = ctypes.c_void_p
     with torch.cuda.device(dev):
-        rc = lib.kda_intra_fwd(ptr(q.data_ptr()), ptr(k.data_ptr()), ptr(g.data_ptr()),
-                               ptr(beta.data_ptr()), ptr(Aqk.data_ptr()), ptr(Akk.data_ptr()),
-                               B, T, H, _DTYPES[q.dtype], _stream_handle(stream, dev))
+        rc = lib.kda_intra_fwd_ex(ptr(q.data_ptr()), ptr(k.data_ptr()), ptr(g.data_ptr()),
+                                  ptr(beta.data_ptr()), ptr(Aqk.data_ptr()),
+                                  ptr(Akk.data_ptr()), B, T, H, _DTYPES[q.dtype],
+                                  ctypes.byref(opts), _stream_handle(stream, dev))
     if rc != KDA_OK:
-        raise KdaError(rc, "kda_intra_fwd")
+        raise KdaError(rc, "kda_intra_fwd_ex")
     return Aqk, Akk
 
 

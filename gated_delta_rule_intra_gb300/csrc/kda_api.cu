@@ -228,31 +228,49 @@ kda_status_t kda_intra_bwd(const void *q, const void *k, const float *g, const f
                                                                         : KDA_ERR_CUDA;
 }
 
-kda_status_t kda_intra_fwd(const void *q, const void *k, const float *g, const float *beta,
-                           float *Aqk, float *Akk, int B, int T, int H, kda_dtype_t qk_dtype,
-                           kda_stream_t stream) {
+kda_status_t kda_intra_fwd_ex(const void *q, const void *k, const float *g, const float *beta,
+                              float *Aqk, float *Akk, int B, int T, int H,
+                              kda_dtype_t qk_dtype, const kda_intra_fwd_opts_t *opts,
+                              kda_stream_t stream) {
+    kda_intra_fwd_opts_t o;
+    memset(&o, 0, sizeof(o));
+    if (opts) o = *opts;
     if (!q || !k || !g || !beta || !Aqk || !Akk) return KDA_ERR_NULL;
-    kda_status_t st = check_shape(B, T, H);
+    const int HV = o.HV ? o.HV : H;
+    if (H <= 0 || HV <= 0 || HV % H != 0) return KDA_ERR_SHAPE;
+    const bool varlen = o.cu_seqlens || o.chunk_indices;
+    if (varlen) {
+        if (!o.cu_seqlens || (!o.chunk_indices && o.num_chunks > 0)) return KDA_ERR_NULL;
+        if (B != 1 || o.num_seqs <= 0 || o.num_chunks < 0) return KDA_ERR_SHAPE;
+        if ((long long)o.num_chunks * HV > 0x7fffffffLL) return KDA_ERR_SHAPE;
+        if ((uintptr_t)o.cu_seqlens % 4u || (uintptr_t)o.chunk_indices % 4u)
+            return KDA_ERR_ALIGN;
+    }
+    kda_status_t st = check_shape(B, T, HV, varlen);
     if (st != KDA_OK) return st;
     if (qk_dtype != KDA_BF16 && qk_dtype != KDA_FP16) return KDA_ERR_DTYPE;
     const void *a16[] = {q, k, g, Aqk, Akk};
     for (const void *p : a16)
         if ((uintptr_t)p % 16u) return KDA_ERR_ALIGN;
     if ((uintptr_t)beta % 4u) return KDA_ERR_ALIGN;
-    const size_t rows = (size_t)B * T * H;
+    const size_t rq = (size_t)B * T * H, rv = (size_t)B * T * HV;
     const Range in[] = {
-        {(uintptr_t)q, (uintptr_t)q + rows * KDA_K * 2},
-        {(uintptr_t)k, (uintptr_t)k + rows * KDA_K * 2},
-        {(uintptr_t)g, (uintptr_t)g + rows * KDA_K * 4},
-        {(uintptr_t)beta, (uintptr_t)beta + rows * 4},
+        {(uintptr_t)q, (uintptr_t)q + rq * KDA_K * 2},
+        {(uintptr_t)k, (uintptr_t)k + rq * KDA_K * 2},
+        {(uintptr_t)g, (uintptr_t)g + rv * KDA_K * 4},
+        {(uintptr_t)beta, (uintptr_t)beta + rv * 4},
+        {(uintptr_t)o.cu_seqlens,
+         varlen ? (uintptr_t)o.cu_seqlens + ((size_t)o.num_seqs + 1) * 4 : 0},
+        {(uintptr_t)o.chunk_indices,
+         varlen ? (uintptr_t)o.chunk_indices + (size_t)o.num_chunks * 8 : 0},
     };
     const Range out[] = {
-        {(uintptr_t)Aqk, (uintptr_t)Aqk + rows * KDA_BT * 4},
-        {(uintptr_t)Akk, (uintptr_t)Akk + rows * KDA_BT * 4},
+        {(uintptr_t)Aqk, (uintptr_t)Aqk + rv * KDA_BT * 4},
+        {(uintptr_t)Akk, (uintptr_t)Akk + rv * KDA_BT * 4},
     };
-    for (const Range &o : out)
+    for (const Range &ob : out)
         for (const Range &r : in)
-            if (overlaps(o, r)) return KDA_ERR_OVERLAP;
+            if (overlaps(ob, r)) return KDA_ERR_OVERLAP;
     if (overlaps(out[0], out[1])) return KDA_ERR_OVERLAP;
     if ((st = check_device()) != KDA_OK) return st;
     (void)cudaGetLastError();
@@ -260,7 +278,18 @@ kda_status_t kda_intra_fwd(const void *q, const void *k, const float *g, const f
     a.q = q; a.k = k; a.g = g; a.beta = beta; a.Aqk = Aqk; a.Akk = Akk;
     a.B = B; a.T = T; a.H = H;
     a.fp16 = (qk_dtype == KDA_FP16);
+    a.HV = HV;
+    a.cu_seqlens = o.cu_seqlens;
+    a.chunk_indices = o.chunk_indices;
+    a.num_seqs = o.num_seqs;
+    a.num_chunks = o.num_chunks;
     return kda::launch_intra_fwd(a, (cudaStream_t)stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_intra_fwd(const void *q, const void *k, const float *g, const float *beta,
+                           float *Aqk, float *Akk, int B, int T, int H, kda_dtype_t qk_dtype,
+                           kda_stream_t stream) {
+    return kda_intra_fwd_ex(q, k, g, beta, Aqk, Akk, B, T, H, qk_dtype, nullptr, stream);
 }
 
 size_t kda_intra_bwd_host_workspace_bytes(int B, int T, int H, kda_dtype_t qk_dtype) {

@@ -48,7 +48,8 @@ constexpr int FM_DIAG = FM_BETA + 512;          // f32 [2][512]: diagonal sums u
 constexpr int FM_BAR = FM_DIAG + 2 * 512 * 4;   // full[2], mma, staging free
 constexpr int FM_CNT = FM_BAR + 32;             // operand counter
 constexpr int FM_TSLOT = FM_CNT + 8;
-constexpr int FM_TOTAL = FM_TSLOT + 8;
+constexpr int FM_META = FM_TSLOT + 8;           // varlen: per stage {first token row, valid rows}
+constexpr int FM_TOTAL = FM_META + 16;
 constexpr int FM_ALLOC = FM_TOTAL + 1024;       // slack for aligning the base
 static_assert(FM_STG % 1024 == 0, "swizzled staging needs 1024-byte alignment");
 static_assert(FM_ALLOC <= 232448, "shared memory");
@@ -79,28 +80,72 @@ struct FwdMaps {
     CUtensorMap q, k, g, aqk, akk;
 };
 
-// One warp queues a unit's copies: 8 swizzled TMA boxes from lane 0, beta as 64
-// four-byte cp.async copies from all lanes.
-template <typename io_t>
+// Options: H in the kernel is the number of heads of g, beta and the outputs (HV); q
+// and k have HV / G heads.  Variable-length launches: unit u is head u % H of chunk
+// chunk_indices[2c+1] of sequence chunk_indices[2c], c = u / H, sequence n being
+// tokens [cu_seqlens[n], cu_seqlens[n+1]).
+struct FwdExtras {
+    int G;
+    const int *cu_seqlens, *chunk_indices;
+    int num_seqs;
+};
+
+// First token row and valid rows (1..64) of a variable-length unit; {0, 0} for an
+// entry that names no chunk of cu_seqlens (the unit is then skipped).
+__device__ __forceinline__ void varlen_rows(long long u, int H, int T, const FwdExtras &ex,
+                                            int &start, int &len) {
+    const size_t c = (size_t)((unsigned)u / (unsigned)H);
+    const int n = __ldg(ex.chunk_indices + 2 * c), j = __ldg(ex.chunk_indices + 2 * c + 1);
+    start = 0;
+    len = 0;
+    if (n >= 0 && n < ex.num_seqs && j >= 0) {
+        const long long bos = __ldg(ex.cu_seqlens + n), eos = __ldg(ex.cu_seqlens + n + 1);
+        const long long st = bos + (long long)BT * j;
+        if (bos >= 0 && st < eos && eos <= T) {
+            start = (int)st;
+            len = (int)(eos - st < BT ? eos - st : BT);
+        }
+    }
+}
+
+// One warp queues a unit's copies: 8 swizzled TMA boxes from lane 0 (rows past the
+// tensor's end are zero-filled), beta as 64 four-byte cp.async copies from all lanes
+// (zero-filled past the unit's valid rows).  A variable-length unit's row range is
+// recorded in `meta` by lane 0 before its arrival on the stage barrier.
+template <typename io_t, bool VARLEN>
 __device__ __forceinline__ void load_unit(unsigned char *st, float *sbeta, uint64_t *full,
-                                          const FwdMaps &tm, const float *__restrict__ beta,
-                                          long long u, int T, int H, int lane) {
-    const Unit x = decode_unit(u, H, T / BT);
-    const int row = x.b * T + x.c * BT;
+                                          int *meta, const FwdMaps &tm,
+                                          const float *__restrict__ beta, long long u, int T,
+                                          int H, const FwdExtras &ex, int lane) {
+    int row, h, len = BT;
+    if constexpr (VARLEN) {
+        varlen_rows(u, H, T, ex, row, len);
+        h = (int)((unsigned)u % (unsigned)H);
+        if (lane == 0) {
+            meta[0] = row;
+            meta[1] = len;
+        }
+    } else {
+        const Unit x = decode_unit(u, H, T / BT);
+        row = x.b * T + x.c * BT;
+        h = x.h;
+    }
     if (lane == 0) {
         tc::mbar_arrive_expect_tx(full, FSTAGE_TX_BYTES);
         for (int b = 0; b < 2; ++b) {
-            tc::tma_load_3d(st + FS_Q + b * 8192, &tm.q, 64 * b, x.h, row, full);
-            tc::tma_load_3d(st + FS_K + b * 8192, &tm.k, 64 * b, x.h, row, full);
+            tc::tma_load_3d(st + FS_Q + b * 8192, &tm.q, 64 * b, h / ex.G, row, full);
+            tc::tma_load_3d(st + FS_K + b * 8192, &tm.k, 64 * b, h / ex.G, row, full);
         }
-        for (int b = 0; b < 4; ++b) tc::tma_load_3d(st + FS_G + b * 8192, &tm.g, 32 * b, x.h, row, full);
+        for (int b = 0; b < 4; ++b) tc::tma_load_3d(st + FS_G + b * 8192, &tm.g, 32 * b, h, row, full);
     }
-    const float *b0 = beta + ((size_t)row * H + x.h);
+    const float *b0 = beta + ((size_t)row * H + h);
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
         const int r = lane + 32 * e;
         const uint32_t s = tc::smem_u32(sbeta + r);
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(b0 + (size_t)r * H)
+        const bool take = r < len;
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(s),
+                     "l"(take ? b0 + (size_t)r * H : beta), "r"(take ? 4 : 0)
                      : "memory");
     }
     tc::cp_async_mbar_arrive_noinc(full);
@@ -142,10 +187,14 @@ __device__ __forceinline__ void ld8_f32(const unsigned char *tile, int r, int c,
     }
 }
 
-template <typename io_t>
+// VARLEN: units from cu_seqlens / chunk_indices.  A unit's rows past its sequence's
+// end never reach a valid output (row r only meets sources s <= r), so nothing is
+// masked on the way in; a short chunk's valid rows leave through plain stores.
+template <typename io_t, bool VARLEN>
 __global__ void __launch_bounds__(FW_THREADS, 1)
 kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restrict__ beta,
-                        int T, int H, long long units) {
+                        float *Aqk, float *Akk, int T, int H, long long units,
+                        const FwdExtras ex) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem =
         smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);  // 1024-aligned
@@ -155,6 +204,7 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
     uint64_t *stg_free = full + 3;  // completes once per unit: the last tiles have left
     uint32_t *ops_count = reinterpret_cast<uint32_t *>(smem + FM_CNT);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + FM_TSLOT);
+    int *meta = reinterpret_cast<int *>(smem + FM_META);
     unsigned char *stg = smem + FM_STG;
     const long long stride = gridDim.x;
 
@@ -183,9 +233,11 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
     if (warp == 0) {
         const long long u0 = blockIdx.x;
         float *sb = reinterpret_cast<float *>(smem + FM_BETA);
-        if (u0 < units) load_unit<io_t>(smem, sb, &full[0], tm, beta, u0, T, H, lane);
+        if (u0 < units)
+            load_unit<io_t, VARLEN>(smem, sb, &full[0], meta, tm, beta, u0, T, H, ex, lane);
         if (u0 + stride < units)
-            load_unit<io_t>(smem + FSTAGE, sb + 64, &full[1], tm, beta, u0 + stride, T, H, lane);
+            load_unit<io_t, VARLEN>(smem + FSTAGE, sb + 64, &full[1], meta + 2, tm, beta,
+                                    u0 + stride, T, H, ex, lane);
     }
 
     const float nan = __int_as_float(0x7fc00000);
@@ -197,6 +249,18 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
         const unsigned char *sq = st + FS_Q, *sk = st + FS_K, *sg = st + FS_G;
         const float *sbeta = reinterpret_cast<const float *>(smem + FM_BETA) + 64 * sidx;
         ok &= tc::mbar_wait(&full[sidx], (uint32_t)(it >> 1) & 1u, SPIN_LIMIT);
+        // the unit's first token row, head and valid rows (read now: the stage's meta
+        // is rewritten by the refill that follows this unit's last barrier)
+        int row, h, len = BT;
+        if constexpr (VARLEN) {
+            row = meta[2 * sidx];
+            len = meta[2 * sidx + 1];
+            h = (int)((unsigned)u % (unsigned)H);
+        } else {
+            const Unit x = decode_unit(u, H, T / BT);
+            row = x.b * T + x.c * BT;
+            h = x.h;
+        }
 
         // ---- prescale: thread = (TMEM lane m, 32 channels).  Lane m < 64 holds the q
         // row m, lane m >= 64 the beta*k row m - 64 (A operand). ----
@@ -237,9 +301,9 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
 #pragma unroll
             for (int j = 0; j < 6; ++j) {
                 const int item = tid + FW_THREADS * j;
-                const int row = item % 96, ch = 4 * (item / 96);
-                const int tt = row < 16 ? 1 : row < 48 ? 2 : 3;
-                const int sr = row - 8 * tt * (tt - 1);  // source row s
+                const int brow = item % 96, ch = 4 * (item / 96);
+                const int tt = brow < 16 ? 1 : brow < 48 ? 2 : 3;
+                const int sr = brow - 8 * tt * (tt - 1);  // source row s
                 const uint2 w = *reinterpret_cast<const uint2 *>(sk + swz<2>(sr, ch));
                 const io_t *kk = reinterpret_cast<const io_t *>(&w);
                 const float4 gs = *reinterpret_cast<const float4 *>(sg + swz<4>(sr, ch));
@@ -427,18 +491,28 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
-        if (tid == 0) {
-            const Unit x = decode_unit(u, H, T / BT);
-            const int row = x.b * T + x.c * BT;
-            tc::tma_store_3d(&tm.aqk, stg, 0, x.h, row);
-            tc::tma_store_3d(&tm.aqk, stg + 8192, 32, x.h, row);
-            tc::tma_store_3d(&tm.akk, stg + 16384, 0, x.h, row);
-            tc::tma_store_3d(&tm.akk, stg + 24576, 32, x.h, row);
+        if (tid == 0 && len == BT) {
+            tc::tma_store_3d(&tm.aqk, stg, 0, h, row);
+            tc::tma_store_3d(&tm.aqk, stg + 8192, 32, h, row);
+            tc::tma_store_3d(&tm.akk, stg + 16384, 0, h, row);
+            tc::tma_store_3d(&tm.akk, stg + 24576, 32, h, row);
             tc::bulk_commit_group();
         }
+        if (VARLEN && len < BT) {  // a short chunk: its valid rows only, by plain stores
+            const int per = len * (BT / 4);
+            for (int x = tid; x < 2 * per; x += FW_THREADS) {
+                const int tensor = x >= per, rem = x - tensor * per;
+                const int r = rem / (BT / 4), c4 = rem % (BT / 4);
+                const float4 v = *reinterpret_cast<const float4 *>(stg + stg_off(tensor, r, 4 * c4));
+                float *dst = (tensor ? Akk : Aqk) + ((size_t)(row + r) * H + h) * BT + 4 * c4;
+                *reinterpret_cast<float4 *>(dst) = v;
+            }
+            __syncthreads();  // the staging is read before the next unit may write it
+        }
         if (warp == 0 && u + 2 * stride < units)
-            load_unit<io_t>(st, reinterpret_cast<float *>(smem + FM_BETA) + 64 * sidx, &full[sidx],
-                            tm, beta, u + 2 * stride, T, H, lane);
+            load_unit<io_t, VARLEN>(st, reinterpret_cast<float *>(smem + FM_BETA) + 64 * sidx,
+                                    &full[sidx], meta + 2 * sidx, tm, beta, u + 2 * stride, T,
+                                    H, ex, lane);
     }
 
     if (tid == 0) tc::bulk_wait_all();
@@ -480,9 +554,9 @@ cudaError_t encode_rows(CUtensorMap *m, CUtensorMapDataType dt, int esize, const
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <typename io_t>
+template <typename io_t, bool VARLEN>
 cudaError_t launch_typed(const FwdArgs &a, cudaStream_t stream) {
-    auto kern = kda_intra_fwd_tc_kernel<io_t>;
+    auto kern = kda_intra_fwd_tc_kernel<io_t, VARLEN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          FM_ALLOC);
     if (e != cudaSuccess) return e;
@@ -495,20 +569,28 @@ cudaError_t launch_typed(const FwdArgs &a, cudaStream_t stream) {
             return e;
         if (dev >= 0 && dev < 64) g_num_sms[dev] = nsm;
     }
-    const cuuint64_t rows = (cuuint64_t)a.B * a.T, H = (cuuint64_t)a.H;
+    const int HV = a.HV > 0 ? a.HV : a.H;
+    const cuuint64_t rows = (cuuint64_t)a.B * a.T, HQ = (cuuint64_t)a.H, H = (cuuint64_t)HV;
     const CUtensorMapDataType io =
         a.fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     FwdMaps tm;
-    if ((e = encode_rows(&tm.q, io, 2, a.q, KD, H, rows)) != cudaSuccess ||
-        (e = encode_rows(&tm.k, io, 2, a.k, KD, H, rows)) != cudaSuccess ||
+    if ((e = encode_rows(&tm.q, io, 2, a.q, KD, HQ, rows)) != cudaSuccess ||
+        (e = encode_rows(&tm.k, io, 2, a.k, KD, HQ, rows)) != cudaSuccess ||
         (e = encode_rows(&tm.g, f32, 4, a.g, KD, H, rows)) != cudaSuccess ||
         (e = encode_rows(&tm.aqk, f32, 4, a.Aqk, BT, H, rows)) != cudaSuccess ||
         (e = encode_rows(&tm.akk, f32, 4, a.Akk, BT, H, rows)) != cudaSuccess)
         return e;
-    const long long units = (long long)a.B * a.H * (a.T / BT);
+    FwdExtras ex;
+    ex.G = HV / a.H;
+    ex.cu_seqlens = a.cu_seqlens;
+    ex.chunk_indices = a.chunk_indices;
+    ex.num_seqs = a.num_seqs;
+    const long long units =
+        VARLEN ? (long long)a.num_chunks * HV : (long long)a.B * HV * (a.T / BT);
+    if (units == 0) return cudaSuccess;
     const unsigned grid = (unsigned)(units < nsm ? units : nsm);
-    kern<<<grid, FW_THREADS, FM_ALLOC, stream>>>(tm, a.beta, a.T, a.H, units);
+    kern<<<grid, FW_THREADS, FM_ALLOC, stream>>>(tm, a.beta, a.Aqk, a.Akk, a.T, HV, units, ex);
     return cudaGetLastError();
 }
 
@@ -516,8 +598,11 @@ cudaError_t launch_typed(const FwdArgs &a, cudaStream_t stream) {
 }  // namespace fwdimpl
 
 cudaError_t launch_intra_fwd(const FwdArgs &a, cudaStream_t stream) {
-    return a.fp16 ? fwdimpl::launch_typed<__half>(a, stream)
-                  : fwdimpl::launch_typed<__nv_bfloat16>(a, stream);
+    if (a.cu_seqlens)
+        return a.fp16 ? fwdimpl::launch_typed<__half, true>(a, stream)
+                      : fwdimpl::launch_typed<__nv_bfloat16, true>(a, stream);
+    return a.fp16 ? fwdimpl::launch_typed<__half, false>(a, stream)
+                  : fwdimpl::launch_typed<__nv_bfloat16, false>(a, stream);
 }
 
 }  // namespace kda

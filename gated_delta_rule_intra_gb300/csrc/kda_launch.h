@@ -29,8 +29,12 @@ struct FwdArgs {
     const void *q, *k;
     const float *g, *beta;
     float *Aqk, *Akk;
-    int B, T, H;
+    int B, T, H;  // H = heads of q and k
     bool fp16;
+    int HV = 0;   // heads of g, beta and the outputs (0 = H); a multiple of H
+    // variable-length sequences, as in BwdArgs
+    const int *cu_seqlens = nullptr, *chunk_indices = nullptr;
+    int num_seqs = 0, num_chunks = 0;
 };
 
 // Tensor-core (tcgen05 TF32) forward kernel.

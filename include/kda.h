@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 4
+#define KDA_ABI_VERSION 5
 #define KDA_BT 64  /* chunk length */
 #define KDA_BC 16  /* sub-block length inside a chunk */
 #define KDA_K 128  /* head dimension */
@@ -208,6 +208,29 @@ kda_status_t kda_intra_fwd(const void *q, const void *k, const float *g,
                            const float *beta, float *Aqk, float *Akk,
                            int B, int T, int H, kda_dtype_t qk_dtype,
                            kda_stream_t stream);
+
+/*
+ * Options of kda_intra_fwd_ex (zero-initialise; a zeroed struct or NULL gives exactly
+ * kda_intra_fwd), with the meanings of kda_intra_bwd_opts_t:
+ *   HV             heads of g, beta, Aqk and Akk; q and k keep H heads, and value head
+ *                  hv reads q/k head hv / (HV / H).  0 means HV = H.
+ *   cu_seqlens,    variable-length sequences packed along T (B == 1, any T >= 1):
+ *   chunk_indices, the same tables and the same checks as for the backward.  Rows of
+ *   num_seqs,      a chunk past its sequence's end take no part in any valid entry and
+ *   num_chunks     are not written; tokens no entry names are left untouched.
+ */
+typedef struct {
+    int HV;
+    const int *cu_seqlens;
+    const int *chunk_indices;
+    int num_seqs;
+    int num_chunks;
+} kda_intra_fwd_opts_t;
+
+kda_status_t kda_intra_fwd_ex(const void *q, const void *k, const float *g,
+                              const float *beta, float *Aqk, float *Akk,
+                              int B, int T, int H, kda_dtype_t qk_dtype,
+                              const kda_intra_fwd_opts_t *opts, kda_stream_t stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *kda_status_str(kda_status_t status);

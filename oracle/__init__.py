@@ -203,3 +203,40 @@ def intra_bwd_varlen(q, k, g, beta, dAqk, dAkk, cu_seqlens, *, dq_in=None, dk_in
         for out, x in zip((dq, dk, db, dg), part):
             out[:, a:b] = x[:, :L]
     return dq, dk, db, dg
+
+
+def intra_fwd_ex(q, k, g, beta, *, cu_seqlens=None, bt: int = 64, nthreads: int = 0, lib=None):
+    """The forward with grouped value heads and variable-length sequences, composed
+    from intra_fwd the same way intra_bwd_ex / intra_bwd_varlen compose the backward
+    (q/k heads repeated; each sequence padded to whole chunks, solved, cut back; rows of
+    tokens outside every sequence come back as NaN)."""
+    q, k, g, beta = _f64(q), _f64(k), _f64(g), _f64(beta)
+    HV, H = g.shape[2], q.shape[2]
+    if HV % H:
+        raise ValueError("HV must be a multiple of H")
+    if HV > H:
+        q = np.repeat(q, HV // H, axis=2)
+        k = np.repeat(k, HV // H, axis=2)
+    if cu_seqlens is None:
+        return intra_fwd(q, k, g, beta, bt=bt, nthreads=nthreads, lib=lib)
+    cu = [int(v) for v in np.asarray(cu_seqlens).reshape(-1)]
+    T = g.shape[1]
+    Aqk = np.full((1, T, HV, bt), np.nan)
+    Akk = np.full((1, T, HV, bt), np.nan)
+    for a, b in zip(cu[:-1], cu[1:]):
+        L = b - a
+        if L <= 0:
+            continue
+        Lp = -(-L // bt) * bt
+
+        def pad(x, edge=False):
+            y = x[:, a:b]
+            fill = np.repeat(y[:, -1:], Lp - L, axis=1) if edge else \
+                np.zeros((1, Lp - L) + y.shape[2:])
+            return np.concatenate([y, fill], axis=1)
+
+        fa, fk = intra_fwd(pad(q), pad(k), pad(g, edge=True), pad(beta), bt=bt,
+                           nthreads=nthreads, lib=lib)
+        Aqk[:, a:b] = fa[:, :L]
+        Akk[:, a:b] = fk[:, :L]
+    return Aqk, Akk

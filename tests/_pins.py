@@ -124,6 +124,33 @@ def ragged_autograd_backward(inp, cu_seqlens, bt):
             t["g"].grad.numpy())
 
 
+def ragged_separable_forward(inp, cu_seqlens, bt):
+    """Aqk, Akk of packed variable-length sequences (B == 1) as [1, T, H, bt] arrays:
+    per chunk, over its valid rows only, (q 2^g)(k 2^-g)^T masked, in torch fp64;
+    rows outside every sequence are NaN."""
+    t = {n: torch.as_tensor(np.asarray(v, dtype=np.float64)) for n, v in inp.items()}
+    T, H = t["g"].shape[1], t["g"].shape[2]
+    Aqk = torch.full((1, T, H, bt), float("nan"), dtype=torch.float64)
+    Akk = torch.full((1, T, H, bt), float("nan"), dtype=torch.float64)
+    cu = [int(v) for v in np.asarray(cu_seqlens).reshape(-1)]
+    for a, b in zip(cu[:-1], cu[1:]):
+        for c0 in range(a, b, bt):
+            m = min(c0 + bt, b) - c0
+            sl = slice(c0, c0 + m)
+            q, k, g = (t[n][0, sl].transpose(0, 1) for n in ("q", "k", "g"))
+            beta = t["beta"][0, sl].transpose(0, 1)
+            lower = torch.tril(torch.ones(m, m, dtype=torch.float64))
+            strict = torch.tril(torch.ones(m, m, dtype=torch.float64), -1)
+            up, dn = torch.exp2(g), torch.exp2(-g)
+            aq = ((q * up) @ (k * dn).transpose(-1, -2)) * lower
+            ak = beta.unsqueeze(-1) * ((k * up) @ (k * dn).transpose(-1, -2)) * strict
+            Aqk[0, sl, :, :] = 0.0
+            Akk[0, sl, :, :] = 0.0
+            Aqk[0, sl, :, :m] = aq.transpose(0, 1)
+            Akk[0, sl, :, :m] = ak.transpose(0, 1)
+    return Aqk.numpy(), Akk.numpy()
+
+
 def ragged_reverse_cumsum(x, cu_seqlens, bt):
     """Inclusive reverse cumsum along tokens inside each (possibly short) chunk of
     packed variable-length sequences, by explicit loops over tokens."""

@@ -265,3 +265,33 @@ def test_fwd_valid_call_reaches_the_device(lib):
     if torch.cuda.is_available():
         pytest.skip("would launch on a real device")
     assert fwd_call(lib) in (ERR_CUDA, ERR_DEVICE)
+
+
+def fwd_ex_call(lib, B=1, T=64, H=1, dtype=0, HV=0, ins=None, **override):
+    ptrs = {n: BASE + i * SPAN for i, n in enumerate(("q", "k", "g", "beta", "Aqk", "Akk"))}
+    ptrs.update(override)
+    vp = ctypes.c_void_p
+    opts = kda.KdaFwdOpts()
+    opts.HV = HV
+    for name, val in (ins or {}).items():
+        setattr(opts, name, val)
+    args = [vp(ptrs[n]) for n in ("q", "k", "g", "beta", "Aqk", "Akk")]
+    return lib.kda_intra_fwd_ex(*args, B, T, H, dtype, ctypes.byref(opts), vp(0))
+
+
+def test_fwd_ex_rejections(lib):
+    assert fwd_ex_call(lib, H=2, HV=3) == ERR_SHAPE
+    assert fwd_ex_call(lib, B=2, T=128, ins=varlen_ins()) == ERR_SHAPE
+    assert fwd_ex_call(lib, ins=varlen_ins(num_seqs=0)) == ERR_SHAPE
+    assert fwd_ex_call(lib, ins=varlen_ins(cu=0)) == ERR_NULL
+    assert fwd_ex_call(lib, ins=varlen_ins(ci=BASE + 11 * SPAN + 2)) == ERR_ALIGN
+    assert fwd_ex_call(lib, ins=varlen_ins(cu=BASE + 4 * SPAN + 64)) == ERR_OVERLAP  # in Aqk
+    assert fwd_ex_call(lib, T=100) == ERR_SHAPE
+
+
+def test_fwd_ex_accepts_groups_and_varlen(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("would launch on a real device")
+    assert fwd_ex_call(lib, H=2, HV=8) in (ERR_CUDA, ERR_DEVICE)
+    assert fwd_ex_call(lib, T=100, ins=varlen_ins()) in (ERR_CUDA, ERR_DEVICE)

@@ -111,3 +111,90 @@ def test_forward_and_backward_satisfy_euler_identities():
     scale2 = (dev["dAkk"].double().abs() * Akk.double().abs()).sum().item()
     assert abs(lhs1 - rhs1) <= 1e-3 * scale1, (lhs1, rhs1)
     assert abs(lhs2 - rhs2) <= 1e-3 * scale2, (lhs2, rhs2)
+
+
+# ---------------------------------------------------------------- options (kda_intra_fwd_ex)
+
+def ref_fwd_ex(cpu, cu=None):
+    return oracle.intra_fwd_ex(*(cpu[n] for n in IN),
+                               cu_seqlens=None if cu is None else cu.numpy())
+
+
+def run_fwd_ex(cpu, cu=None, chunk_indices=None, **kw):
+    dev = _gpu.to_device({n: cpu[n] for n in IN})
+    extra = {}
+    if cu is not None:
+        extra["cu_seqlens"] = cu.cuda()
+        if chunk_indices is not None:
+            extra["chunk_indices"] = chunk_indices.cuda()
+    return kda.kda_intra_fwd(*(dev[n] for n in IN), **extra, **kw)
+
+
+@pytest.mark.parametrize("G", [2, 4])
+def test_grouped_value_heads(G):
+    x = kda_inputs.make_inputs(2, 192, 2 * G, seed=90 + G)
+    x["q"] = x["q"][:, :, ::G].contiguous()
+    x["k"] = x["k"][:, :, ::G].contiguous()
+    assert_fwd_close(run_fwd_ex(x), ref_fwd_ex(x), f"fwd GVA G={G}")
+
+
+VARLEN_LENS = [1, 63, 64, 65, 127, 128, 129, 200, 7, 300, 2, 511]
+
+
+@pytest.mark.parametrize("qk_dtype,gate_lo", [(torch.bfloat16, -0.5), (torch.float16, -8.0)])
+def test_varlen(qk_dtype, gate_lo):
+    cpu, cu = kda_inputs.make_varlen_inputs(VARLEN_LENS, 3, gate_lo=gate_lo, qk_dtype=qk_dtype,
+                                            seed=94)
+    assert_fwd_close(run_fwd_ex(cpu, cu), ref_fwd_ex(cpu, cu), f"fwd varlen {qk_dtype}")
+
+
+def test_varlen_with_groups():
+    cpu, cu = kda_inputs.make_varlen_inputs(VARLEN_LENS[:8], 4, HQ=2, seed=95)
+    assert_fwd_close(run_fwd_ex(cpu, cu), ref_fwd_ex(cpu, cu), "fwd varlen GVA")
+
+
+def test_varlen_whole_chunks_match_the_fixed_length_kernel_bitwise():
+    cpu, cu = kda_inputs.make_varlen_inputs([128, 64, 320], 2, seed=96)
+    a = run_fwd_ex(cpu, cu)
+    b = run_fwd(cpu)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_varlen_foreign_rows_untouched():
+    """Tokens after the last sequence carry NaN / huge inputs; the outputs start as a
+    canary: valid rows match the oracle, rows outside every sequence stay canary."""
+    lens = [70, 33, 100]
+    cpu, cu = kda_inputs.make_varlen_inputs(lens + [90], 2, seed=97)
+    n = sum(lens)
+    cu = cu[:-1].clone()
+    for name in ("q", "k", "beta"):
+        cpu[name][0, n:] = float("nan")
+    cpu["g"][0, n:] = 3e38
+    T = cpu["g"].shape[1]
+    canary = -5.5
+    Aqk = torch.full((1, T, 2, 64), canary, device="cuda")
+    Akk = torch.full((1, T, 2, 64), canary, device="cuda")
+    got = run_fwd_ex(cpu, cu, Aqk=Aqk, Akk=Akk)
+    ref = ref_fwd_ex(cpu, cu)
+    assert_fwd_close([x[:, :n] for x in got], [r[:, :n] for r in ref], "fwd varlen poisoned")
+    for x in got:
+        assert bool((x[:, n:] == canary).all())
+
+
+def test_varlen_invalid_entries_skipped():
+    cpu, cu = kda_inputs.make_varlen_inputs([100, 64], 1, seed=98)
+    bad = torch.tensor([[0, 0], [5, 0], [0, 2], [-1, 0], [1, -3]], dtype=torch.int32)
+    T = cpu["g"].shape[1]
+    Aqk = torch.full((1, T, 1, 64), 2.5, device="cuda")
+    Akk = torch.full((1, T, 1, 64), 2.5, device="cuda")
+    got = run_fwd_ex(cpu, cu, chunk_indices=bad, Aqk=Aqk, Akk=Akk)
+    ref = ref_fwd_ex(cpu, cu)
+    assert_fwd_close([x[:, :64] for x in got], [r[:, :64] for r in ref], "valid entry")
+    for x in got:
+        assert bool((x[:, 64:] == 2.5).all())
+
+
+def test_varlen_workload_full_size():
+    cpu, cu = kda_inputs.make_varlen_workload()
+    assert_fwd_close(run_fwd_ex(cpu, cu), ref_fwd_ex(cpu, cu), "fwd varlen workload")

@@ -191,3 +191,15 @@ def test_varlen_rows_outside_every_sequence_are_nan(lib):
     inp, _ = _varlen_tiny(lens=[5, 7], seed=14)
     got = oracle.intra_bwd_varlen(*(inp[n] for n in _ARGS), np.array([0, 5, 9]), bt=8, lib=lib)
     assert np.isnan(got[0][0, 9:]).all() and np.isfinite(got[0][0, :9]).all()
+
+
+def test_forward_varlen_and_groups_against_ragged_separable_forward(lib):
+    """The forward's composition (GVA + ragged chunks) against the per-chunk separable
+    forward over valid rows only."""
+    inp, cu = _varlen_tiny(H=4, HQ=2, seed=15, gate_lo=-2.0)
+    got = oracle.intra_fwd_ex(inp["q"], inp["k"], inp["g"], inp["beta"], cu_seqlens=cu, bt=8,
+                              lib=lib)
+    rep = dict(inp, q=np.repeat(inp["q"], 2, axis=2), k=np.repeat(inp["k"], 2, axis=2))
+    want = _pins.ragged_separable_forward(rep, cu, 8)
+    for a, b in zip(got, want):
+        assert _pins.rel_err(a, b) < 1e-12
