@@ -99,6 +99,10 @@ kda_intra_bwd_fp32_kernel(const __grid_constant__ TmaMaps tm, const float *__res
 #pragma unroll
         for (int r = 0; r < BC; ++r) accq[r] = acck[r] = 0.f;
         if (i > 0) {
+            // packed FP32x2 partial sums over even / odd source columns
+            float2 pq[BC], pk[BC];
+#pragma unroll
+            for (int r = 0; r < BC; ++r) pq[r] = pk[r] = make_float2(0.f, 0.f);
             for (int j = 0; j < i; ++j) {
                 const float ge = sg[BC * (j + 1) * KD + d];
                 const float cj = (j == i - 1) ? 1.f : ex2(g2[0].x - ge);  // 2^(g_16i - g_e(j))
@@ -112,14 +116,20 @@ kda_intra_bwd_fp32_kernel(const __grid_constant__ TmaMaps tm, const float *__res
                         const int s = BC * j + 4 * c4 + x;
                         kv[x] = to_f32(sk[s * KD + d]) * ex2(ge - sg[s * KD + d]) * cj;
                     }
+                    const float2 k01 = make_float2(kv[0], kv[1]), k23 = make_float2(kv[2], kv[3]);
 #pragma unroll
                     for (int r = 0; r < BC; ++r) {
                         const float4 aq = *reinterpret_cast<const float4 *>(bq + c4 * 64 + rowoff(r));
                         const float4 ak = *reinterpret_cast<const float4 *>(bk + c4 * 64 + rowoff(r));
-                        accq[r] = fmaf(aq.x, kv[0], fmaf(aq.y, kv[1], fmaf(aq.z, kv[2], fmaf(aq.w, kv[3], accq[r]))));
-                        acck[r] = fmaf(ak.x, kv[0], fmaf(ak.y, kv[1], fmaf(ak.z, kv[2], fmaf(ak.w, kv[3], acck[r]))));
+                        pq[r] = __ffma2_rn(make_float2(aq.z, aq.w), k23, __ffma2_rn(make_float2(aq.x, aq.y), k01, pq[r]));
+                        pk[r] = __ffma2_rn(make_float2(ak.z, ak.w), k23, __ffma2_rn(make_float2(ak.x, ak.y), k01, pk[r]));
                     }
                 }
+            }
+#pragma unroll
+            for (int r = 0; r < BC; ++r) {
+                accq[r] = pq[r].x + pq[r].y;
+                acck[r] = pk[r].x + pk[r].y;
             }
 #pragma unroll
             for (int r = 1; r < BC; ++r) {  // 2^(g_r - g_16i); 1 for r = 0
