@@ -6,6 +6,7 @@ import torch
 
 import gated_delta_rule_intra_gb300 as kda
 import kda_inputs
+import oracle
 from tests import _gpu
 
 pytestmark = pytest.mark.gpu
@@ -199,3 +200,47 @@ def test_sampled_units_match_full_launch():
     cpu = kda_inputs.make_config_inputs(1)
     dev = _gpu.to_device(cpu)
     _gpu.sampled_parity("kda_intra_bwd", 1, cpu, dev, n_units=8)
+
+
+def _device_inputs(B, T, H, seed):
+    """The input recipe of kda_inputs, drawn on the GPU (for sizes too large to draw on
+    the host in reasonable time)."""
+    gen = torch.Generator(device="cuda").manual_seed(seed)
+    f32 = torch.float32
+
+    def rows(x):
+        return (x / x.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+
+    q = rows(torch.randn(B, T, H, 128, generator=gen, device="cuda"))
+    k = rows(torch.randn(B, T, H, 128, generator=gen, device="cuda"))
+    step = torch.rand(B, T, H, 128, generator=gen, device="cuda") * -0.5
+    g = step.view(B, T // 64, 64, H, 128).cumsum(2, dtype=f32).view(B, T, H, 128)
+    del step
+    beta = torch.rand(B, T, H, generator=gen, device="cuda")
+    lower, strict = (m.cuda() for m in kda_inputs.chunk_masks())
+    dAqk = (torch.randn(B, T // 64, 64, H, 64, generator=gen, device="cuda") *
+            lower.view(1, 1, 64, 1, 64)).view(B, T, H, 64)
+    dAkk = (torch.randn(B, T // 64, 64, H, 64, generator=gen, device="cuda") *
+            strict.view(1, 1, 64, 1, 64)).view(B, T, H, 64)
+    return dict(q=q, k=k, g=g.contiguous(), beta=beta, dAqk=dAqk.contiguous(),
+                dAkk=dAkk.contiguous())
+
+
+def test_maximum_head_count():
+    """H = KDA_MAX_H = 65536 (one chunk, 65536 units, about 430 per SM): sampled heads of
+    every output of both backward paths and of the forward against the oracle."""
+    B, T, H = 1, 64, 65536
+    dev = _device_inputs(B, T, H, seed=31)
+    heads = [0, 1, 12345, 40000, H - 2, H - 1]
+    sub = {n: v[:, :, heads].cpu().contiguous() for n, v in dev.items()}
+    ref = _gpu.oracle_outputs(sub)
+    for path in _gpu.PATHS:
+        outs = _gpu.run(path, dev)
+        got = [o[:, :, heads].cpu() for o in outs]
+        del outs
+        _gpu.assert_close(got, ref, _gpu.TOL[path], f"{path} at H = {H}")
+    fref = oracle.intra_fwd(*(sub[n] for n in ("q", "k", "g", "beta")))
+    fouts = kda.kda_intra_fwd(*(dev[n] for n in ("q", "k", "g", "beta")))
+    for name, a, b in zip(("Aqk", "Akk"), fouts, fref):
+        a = a[:, :, heads].double().cpu().numpy()
+        assert float(np.max(np.abs(a - b)) / np.max(np.abs(b))) <= 2e-3, name
