@@ -285,10 +285,19 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
                         const float4 gb =
                             *reinterpret_cast<const float4 *>(sg + swz<4>(16 * t, ch + 4 * q4));
                         const int o = 8 * c + 4 * q4;
-                        v[o + 0] = to_f32(e[4 * q4 + 0]) * scale * ex2(gr.x - gb.x);
-                        v[o + 1] = to_f32(e[4 * q4 + 1]) * scale * ex2(gr.y - gb.y);
-                        v[o + 2] = to_f32(e[4 * q4 + 2]) * scale * ex2(gr.z - gb.z);
-                        v[o + 3] = to_f32(e[4 * q4 + 3]) * scale * ex2(gr.w - gb.w);
+                        const float2 s2 = make_float2(scale, scale);
+                        const float2 d01 = __ffma2_rn(make_float2(gb.x, gb.y), make_float2(-1.f, -1.f), make_float2(gr.x, gr.y));
+                        const float2 d23 = __ffma2_rn(make_float2(gb.z, gb.w), make_float2(-1.f, -1.f), make_float2(gr.z, gr.w));
+                        const float2 x01 = __fmul2_rn(
+                            __fmul2_rn(make_float2(to_f32(e[4 * q4 + 0]), to_f32(e[4 * q4 + 1])), s2),
+                            make_float2(ex2(d01.x), ex2(d01.y)));
+                        const float2 x23 = __fmul2_rn(
+                            __fmul2_rn(make_float2(to_f32(e[4 * q4 + 2]), to_f32(e[4 * q4 + 3])), s2),
+                            make_float2(ex2(d23.x), ex2(d23.y)));
+                        v[o + 0] = x01.x;
+                        v[o + 1] = x01.y;
+                        v[o + 2] = x23.x;
+                        v[o + 3] = x23.y;
                     }
                 }
                 tc::tmem_st16(tl + (uint32_t)(d0 + 16 * h), v);
@@ -308,10 +317,13 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
                 const io_t *kk = reinterpret_cast<const io_t *>(&w);
                 const float4 gs = *reinterpret_cast<const float4 *>(sg + swz<4>(sr, ch));
                 const float4 gt = *reinterpret_cast<const float4 *>(sg + swz<4>(BC * tt, ch));
-                const float4 o = make_float4(to_f32(kk[0]) * ex2(gt.x - gs.x),
-                                             to_f32(kk[1]) * ex2(gt.y - gs.y),
-                                             to_f32(kk[2]) * ex2(gt.z - gs.z),
-                                             to_f32(kk[3]) * ex2(gt.w - gs.w));
+                const float2 d01 = __ffma2_rn(make_float2(gs.x, gs.y), make_float2(-1.f, -1.f), make_float2(gt.x, gt.y));
+                const float2 d23 = __ffma2_rn(make_float2(gs.z, gs.w), make_float2(-1.f, -1.f), make_float2(gt.z, gt.w));
+                const float2 o01 = __fmul2_rn(make_float2(to_f32(kk[0]), to_f32(kk[1])),
+                                              make_float2(ex2(d01.x), ex2(d01.y)));
+                const float2 o23 = __fmul2_rn(make_float2(to_f32(kk[2]), to_f32(kk[3])),
+                                              make_float2(ex2(d23.x), ex2(d23.y)));
+                const float4 o = make_float4(o01.x, o01.y, o23.x, o23.y);
                 *reinterpret_cast<float4 *>(smem + FM_B + boff(tt) + (ch >> 2) * 256 * tt +
                                             (sr >> 3) * 128 + (sr & 7) * 16) = o;
             }

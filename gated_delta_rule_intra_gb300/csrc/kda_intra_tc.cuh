@@ -400,38 +400,66 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         float c2 = 0.f, c3 = 0.f;  // 2^(g_16(i+2) - g_e(i)), 2^(g_16(i+3) - g_e(i))
         if (i < NBLK - 1) {
             const float ge = gsel(r0 + BC, sg[(r0 + BC) * KD + d]);
+            const float2 ge2 = make_float2(ge, ge), m1 = make_float2(-1.f, -1.f);
             float a[BC], v[BC];
 #pragma unroll
-            for (int s = 0; s < BC; ++s) {
-                a[s] = ex2(ge - KDA_EL(g2, s));
-                v[s] = KDA_EL(k2, s) * a[s];
+            for (int m = 0; m < BC / 2; ++m) {
+                const float2 df = __ffma2_rn(g2[m], m1, ge2);
+                a[2 * m] = ex2(df.x);
+                a[2 * m + 1] = ex2(df.y);
+                const float2 vv = __fmul2_rn(k2[m], make_float2(a[2 * m], a[2 * m + 1]));
+                v[2 * m] = vv.x;
+                v[2 * m + 1] = vv.y;
             }
             tc::tmem_st16(tlane + TM_FA + 16 * i, a);
             tc::tmem_st16(tlane + tm_arow(i + 1) + 16 * i, v);
             if (i + 2 < NBLK) {
                 c2 = ex2(gsel(r0 + 2 * BC, sg[(r0 + 2 * BC) * KD + d]) - ge);
 #pragma unroll
-                for (int s = 0; s < BC; ++s) a[s] = v[s] * c2;
+                for (int m = 0; m < BC / 2; ++m) {
+                    const float2 t = __fmul2_rn(make_float2(v[2 * m], v[2 * m + 1]), make_float2(c2, c2));
+                    a[2 * m] = t.x;
+                    a[2 * m + 1] = t.y;
+                }
                 tc::tmem_st16(tlane + tm_arow(i + 2) + 16 * i, a);
             }
             if (i + 3 < NBLK) {
                 c3 = ex2(gsel(r0 + 3 * BC, sg[(r0 + 3 * BC) * KD + d]) - ge);
 #pragma unroll
-                for (int s = 0; s < BC; ++s) a[s] = v[s] * c3;
+                for (int m = 0; m < BC / 2; ++m) {
+                    const float2 t = __fmul2_rn(make_float2(v[2 * m], v[2 * m + 1]), make_float2(c3, c3));
+                    a[2 * m] = t.x;
+                    a[2 * m + 1] = t.y;
+                }
                 tc::tmem_st16(tlane + tm_arow(i + 3) + 16 * i, a);
             }
         }
         if (i > 0) {
             float b[BC], v[BC];
-            b[0] = 1.f;
+            const float2 g0 = make_float2(-g2[0].x, -g2[0].x), p1 = make_float2(1.f, 1.f);
 #pragma unroll
-            for (int r = 1; r < BC; ++r) b[r] = ex2(KDA_EL(g2, r) - g2[0].x);
+            for (int m = 0; m < BC / 2; ++m) {
+                const float2 df = __ffma2_rn(g2[m], p1, g0);
+                b[2 * m] = m == 0 ? 1.f : ex2(df.x);
+                b[2 * m + 1] = ex2(df.y);
+            }
             tc::tmem_st16(tlane + TM_FB + 16 * (i - 1), b);
 #pragma unroll
-            for (int r = 0; r < BC; ++r) v[r] = to_f32(sq[(r0 + r) * KD + d]) * b[r];
+            for (int m = 0; m < BC / 2; ++m) {
+                const float2 t = __fmul2_rn(make_float2(to_f32(sq[(r0 + 2 * m) * KD + d]),
+                                                        to_f32(sq[(r0 + 2 * m + 1) * KD + d])),
+                                            make_float2(b[2 * m], b[2 * m + 1]));
+                v[2 * m] = t.x;
+                v[2 * m + 1] = t.y;
+            }
             tc::tmem_st16(tlane + TM_AQB + 16 * (i - 1), v);
 #pragma unroll
-            for (int r = 0; r < BC; ++r) v[r] = sbeta[r0 + r] * KDA_EL(k2, r) * b[r];
+            for (int m = 0; m < BC / 2; ++m) {
+                const float2 bk = __fmul2_rn(*reinterpret_cast<const float2 *>(sbeta + r0 + 2 * m), k2[m]);
+                const float2 t = __fmul2_rn(bk, make_float2(b[2 * m], b[2 * m + 1]));
+                v[2 * m] = t.x;
+                v[2 * m + 1] = t.y;
+            }
             tc::tmem_st16(tlane + TM_AKBB + 16 * (i - 1), v);
         }
 
