@@ -30,8 +30,12 @@
 //     P_j[d, s] = sum_{r in blk j} q[r,d] 2^(g_r - g_16j) dAqk[r,s]
 //               + beta_r k[r,d] 2^(g_r - g_16j) dAkk[r,s]        (s < 16j)
 //     dkt_cross[s,d] = 2^(g_e(i) - g_s) * sum_{j>i} 2^(g_16j - g_e(i)) P_j[d, s].
-// The 16x16 diagonal blocks run on the FP32 pipes with one exp2 per (r, s, d),
-// two source rows at a time in packed FP32x2 arithmetic.
+// The 16x16 diagonal blocks run on the FP32 pipes, two source rows at a time in
+// packed FP32x2 arithmetic.  Their lower-left 8x8 quadrant (rows 8..15 against
+// sources 0..7) is factorized through row 8 of the block,
+//     2^(g_r - g_s) = 2^(g_r - g_8) * 2^(g_8 - g_s),  both exponents <= 0,
+// so it costs four FMAs per (r, s, d); the two 8x8 triangles left take one exp2
+// per (r, s, d).
 #pragma once
 
 #include <cuda.h>
@@ -529,11 +533,12 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             cp_async_commit();
         }
 
-        // ---- diagonal block: one exp2 per (r, s, d), shared by both sides, two source
-        // rows at a time in packed FP32x2.  Rows run in descending order: once row r is
-        // processed, its row sums and its column sum dkt[r] are complete, so each row is
-        // written out right away.  Rows 15..8 (92 of the 120 pairs) run before the MMA
-        // result is needed; rows 7..0 after it. ----
+        // ---- diagonal block, two source rows at a time in packed FP32x2: one exp2 per
+        // (r, s, d), shared by both sides, in the two 8x8 triangles; the factorized
+        // quadrant in between.  Rows run in descending order: once row r is processed,
+        // its row sums and its column sum dkt[r] are complete, so each row is written
+        // out right away.  Rows 15..8 (92 of the 120 pairs, the quadrant among them) run
+        // before the MMA result is needed; rows 7..0 after it. ----
         float accq[BC], acck[BC], dbv[BC];
         float2 dkt2[BC / 2];
 #pragma unroll
@@ -551,6 +556,19 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         const size_t obase = orow0 * KD + d;
         const uint32_t hk = (uint32_t)H * KD;
 
+        // Lower-left quadrant (rows 8..15 against sources 0..7) factorized through
+        // row 8: 2^(g_r - g_s) = 2^(g_r - g_8) 2^(g_8 - g_s), both exponents <= 0.
+        // kbq[m] holds k_s 2^(g_8 - g_s) for the source pair m; dktq[m] the column
+        // sums still to be scaled by 2^(g_8 - g_s).
+        const float g8 = KDA_EL(g2, BC / 2);
+        float2 kbq[BC / 4], dktq[BC / 4];
+#pragma unroll
+        for (int m = 0; m < BC / 4; ++m) {
+            const float2 df = __ffma2_rn(g2[m], neg1, make_float2(g8, g8));
+            kbq[m] = __fmul2_rn(k2[m], make_float2(ex2(df.x), ex2(df.y)));
+            dktq[m] = make_float2(0.f, 0.f);
+        }
+
         auto diag_row = [&](const int r) {
             const float gv = KDA_EL(g2, r), kv = KDA_EL(k2, r);
             const float qv = to_f32(sq[(r0 + r) * KD + d]);
@@ -561,10 +579,34 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             float2 aacc = make_float2(0.f, 0.f), kacc = make_float2(0.f, 0.f);
             // row r's 16-byte chunk c of the diagonal block sits at c*64 + roff floats
             const int roff = (r >> 3) * 32 + (r & 7) * 4;
+            int cfirst = 0;
+            if (r >= BC / 2) {  // the factorized quadrant: sources 0..7
+                const float ar = r == BC / 2 ? 1.f : ex2(gv - g8);
+                const float2 qa = make_float2(ar * qv, ar * qv);
+                const float2 kba = make_float2(ar * kbr, ar * kbr);
+                float2 sq2 = make_float2(0.f, 0.f), sk2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const float4 aq4 = *reinterpret_cast<const float4 *>(dgq + c * 64 + roff);
+                    const float4 ak4 = *reinterpret_cast<const float4 *>(dgk + c * 64 + roff);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int m = 2 * c + h;
+                        const float2 aq = h ? make_float2(aq4.z, aq4.w) : make_float2(aq4.x, aq4.y);
+                        const float2 ak = h ? make_float2(ak4.z, ak4.w) : make_float2(ak4.x, ak4.y);
+                        sq2 = __ffma2_rn(aq, kbq[m], sq2);
+                        sk2 = __ffma2_rn(ak, kbq[m], sk2);
+                        dktq[m] = __ffma2_rn(ak, kba, __ffma2_rn(aq, qa, dktq[m]));
+                    }
+                }
+                accq[r] = ar * (sq2.x + sq2.y);
+                acck[r] = ar * (sk2.x + sk2.y);
+                cfirst = 2;
+            }
             // pairs (2m, 2m+1) cover s < r; for odd r the last pair is (r-1, r) and
             // carries the diagonal term (E = 1, dAkk[r][r] outside the support -> 0)
 #pragma unroll
-            for (int c = 0; c < (r + 3) / 4; ++c) {
+            for (int c = cfirst; c < (r + 3) / 4; ++c) {
                 const float4 aq4 = *reinterpret_cast<const float4 *>(dgq + c * 64 + roff);
                 const float4 ak4 = *reinterpret_cast<const float4 *>(dgk + c * 64 + roff);
 #pragma unroll
@@ -664,9 +706,11 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         fetch_in(BC - 2);
         fetch_in(BC - 3);
 #pragma unroll
-        for (int r = BC - 1; r >= BC / 2; --r) {
-            accq[r] = acck[r] = 0.f;
-            diag_row(r);
+        for (int r = BC - 1; r >= BC / 2; --r) diag_row(r);
+#pragma unroll
+        for (int m = 0; m < BC / 4; ++m) {
+            const float2 df = __ffma2_rn(g2[m], neg1, make_float2(g8, g8));
+            dkt2[m] = __ffma2_rn(make_float2(ex2(df.x), ex2(df.y)), dktq[m], dkt2[m]);
         }
 
         // ---- cross terms: wait for the MMAs, apply the post-factors ----
