@@ -96,7 +96,8 @@ class VarlenWorkload:
 
 KERNEL_SOURCES = {
     "kda_intra_bwd_tc_kernel": ("kda_intra_tc.cuh", "kda_intra_tc.cu", "tc_ptx.cuh", "kda_common.cuh"),
-    "kda_intra_bwd_fp32_kernel": ("kda_intra_fp32.cu", "kda_common.cuh"),
+    "kda_intra_bwd_fp32_kernel": ("kda_intra_fp32.cu", "kda_intra_tc.cuh", "tc_ptx.cuh",
+                                  "kda_common.cuh"),
     "kda_intra_fwd_tc_kernel": ("kda_intra_fwd_tc.cu", "tc_ptx.cuh", "kda_common.cuh"),
 }
 
@@ -371,10 +372,10 @@ def run_ours(args, cfg):
     ins = [x[n] for n in ("q", "k", "g", "beta", "dAqk", "dAkk")]
     fwd = args.path == "kda_intra_fwd"
     extended = (args.gva > 1 or args.accumulate or args.fold_dg or args.io_dtype_out
-                or args.varlen)
+                or args.varlen or args.factor_diag)
     opts = None
     if fwd:
-        if args.accumulate or args.fold_dg or args.io_dtype_out:
+        if args.accumulate or args.fold_dg or args.io_dtype_out or args.factor_diag:
             raise SystemExit("the forward takes --gva and --varlen only")
         outs = list(kda.kda_intra_fwd(*ins[:4], **varlen))
         if extended:
@@ -383,6 +384,8 @@ def run_ours(args, cfg):
         def step():
             kda.kda_intra_fwd(*ins[:4], *outs, **varlen, stream=stream)
     elif extended:
+        if args.path != "kda_intra_bwd":
+            raise SystemExit("options run on the tensor-core path (--path kda_intra_bwd) only")
         gen = torch.Generator().manual_seed(seed + 1)
         extra = dict(varlen)
         if args.accumulate:
@@ -390,11 +393,12 @@ def run_ours(args, cfg):
             extra.update({n: torch.randn(*shp, generator=gen).to(dev)
                           for n in ("dq_in", "dk_in", "dg_in")})
             extra["db_in"] = torch.randn(cfg.B, cfg.T, cfg.H, generator=gen).to(dev)
+        extra["factor_diag"] = args.factor_diag
         outs = list(kda.kda_intra_bwd_ex(*ins, **extra, fold_dg=args.fold_dg,
                                          dqdk_io_dtype=args.io_dtype_out))
         opts = {"value_heads_per_qk_head": args.gva, "accumulate": args.accumulate,
                 "fold_dg": args.fold_dg, "dqdk_io_dtype": args.io_dtype_out,
-                "varlen": args.varlen}
+                "varlen": args.varlen, "factor_diag": args.factor_diag}
 
         def step():
             kda.kda_intra_bwd_ex(*ins, *outs, **extra, fold_dg=args.fold_dg,
@@ -485,7 +489,8 @@ def run_ours(args, cfg):
     achieved = bytes_per_launch / (ms / args.steps / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
     kname = KERNEL_NAMES[args.path]
-    traffic = ncu_traffic(kname, cfg.name)
+    # the committed summaries cover the plain launch of each path only
+    traffic = None if extended else ncu_traffic(kname, cfg.name)
     line = {
         "metric": METRIC,
         "value": world * cfg.tokens_heads / (ms_per_step / 1e3),
@@ -532,6 +537,9 @@ def main():
     p.add_argument("--varlen", action="store_true",
                    help="the variable-length workload (32768 tokens x 16 heads in "
                         "sequences of log-uniform length) through cu_seqlens")
+    p.add_argument("--factor-diag", action="store_true",
+                   help="diagonal blocks' lower-left quadrant factorized through row 8 "
+                        "(kda_intra_bwd_ex)")
     args = p.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     cfg = kda_inputs.CONFIGS[args.config]

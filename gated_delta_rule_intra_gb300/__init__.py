@@ -44,7 +44,8 @@ class KdaOpts(ctypes.Structure):
                 ("dg_in", ctypes.c_void_p), ("db_in", ctypes.c_void_p),
                 ("fold_dg", ctypes.c_int), ("dqdk_io_dtype", ctypes.c_int),
                 ("cu_seqlens", ctypes.c_void_p), ("chunk_indices", ctypes.c_void_p),
-                ("num_seqs", ctypes.c_int), ("num_chunks", ctypes.c_int)]
+                ("num_seqs", ctypes.c_int), ("num_chunks", ctypes.c_int),
+                ("factor_diag", ctypes.c_int)]
 
 
 class KdaFwdOpts(ctypes.Structure):
@@ -214,7 +215,7 @@ def prepare_chunk_indices(cu_seqlens, bt: int = BT):
 def kda_intra_bwd_ex(q, k, g, beta, dAqk, dAkk, dq=None, dk=None, db=None, dg=None, *,
                      dq_in=None, dk_in=None, dg_in=None, db_in=None, fold_dg=False,
                      dqdk_io_dtype=False, cu_seqlens=None, chunk_indices=None,
-                     stream=None):
+                     factor_diag=False, stream=None):
     """Intra-chunk backward with the extended options of ``kda_intra_bwd_ex``.
 
     q, k have H heads; g, beta, dAqk, dAkk, the outputs and the optional incoming
@@ -225,6 +226,9 @@ def kda_intra_bwd_ex(q, k, g, beta, dAqk, dAkk, dq=None, dk=None, db=None, dg=No
     ``cu_seqlens`` (int32 [N + 1] on the device, B must be 1) packs N sequences of any
     length along T; ``chunk_indices`` (int32 [num_chunks, 2] on the device) defaults to
     ``prepare_chunk_indices(cu_seqlens)``, which reads cu_seqlens on the host.
+    ``factor_diag`` factorizes the lower-left 8x8 quadrant of each diagonal 16x16 block
+    through the block's row 8 (every exponent stays <= 0) instead of one exp2 per
+    (r, s, d); faster, equal up to rounding.
     Returns (dq, dk, db, dg).
     """
     if q.device.type != "cuda":
@@ -260,6 +264,7 @@ def kda_intra_bwd_ex(q, k, g, beta, dAqk, dAkk, dq=None, dk=None, db=None, dg=No
             setattr(opts, name, t.data_ptr())
     opts.fold_dg = int(bool(fold_dg))
     opts.dqdk_io_dtype = int(bool(dqdk_io_dtype))
+    opts.factor_diag = int(bool(factor_diag))
     _varlen_opts(opts, cu_seqlens, chunk_indices, dev)
     lib = load_library()
     ptr = ctypes.c_void_p

@@ -107,6 +107,7 @@ kda_status_t check_ex(const void *q, const void *k, const float *g, const float 
     if (o.fold_dg != 0 && o.fold_dg != 1) return KDA_ERR_OPTION;
     if (o.dqdk_io_dtype != 0 && o.dqdk_io_dtype != 1) return KDA_ERR_OPTION;
     if (o.dqdk_io_dtype && HV != H) return KDA_ERR_OPTION;
+    if (o.factor_diag != 0 && o.factor_diag != 1) return KDA_ERR_OPTION;
     const void *a16[] = {q, k, g, dAqk, dAkk, dq, dk, dg};
     for (const void *p : a16)
         if ((uintptr_t)p % 16u) return KDA_ERR_ALIGN;
@@ -206,6 +207,7 @@ kda_status_t kda_intra_bwd_ex(const void *q, const void *k, const float *g,
     a.db_in = o.db_in;
     a.fold_dg = o.fold_dg != 0;
     a.emit_io = o.dqdk_io_dtype != 0;
+    a.factor_diag = o.factor_diag != 0;
     a.cu_seqlens = o.cu_seqlens;
     a.chunk_indices = o.chunk_indices;
     a.num_seqs = o.num_seqs;

@@ -1,6 +1,6 @@
 // Host side of the tensor-core kernel: tensor maps, the SM count, and the dispatch
-// to the instantiations per q/k element type and sequence layout
-// (kda_intra_tc_{bf16,fp16}[_varlen].cu).
+// to the instantiations per q/k element type, sequence layout and diagonal-block
+// form (kda_intra_tc_{bf16,fp16}[_varlen][_fd].cu).
 #include "kda_intra_tc.cuh"
 
 namespace kda {
@@ -9,6 +9,10 @@ cudaError_t launch_tc_bf16(const BwdArgs &a, cudaStream_t stream);
 cudaError_t launch_tc_fp16(const BwdArgs &a, cudaStream_t stream);
 cudaError_t launch_tc_bf16_varlen(const BwdArgs &a, cudaStream_t stream);
 cudaError_t launch_tc_fp16_varlen(const BwdArgs &a, cudaStream_t stream);
+cudaError_t launch_tc_bf16_fd(const BwdArgs &a, cudaStream_t stream);
+cudaError_t launch_tc_fp16_fd(const BwdArgs &a, cudaStream_t stream);
+cudaError_t launch_tc_bf16_varlen_fd(const BwdArgs &a, cudaStream_t stream);
+cudaError_t launch_tc_fp16_varlen_fd(const BwdArgs &a, cudaStream_t stream);
 
 namespace tcimpl {
 namespace {
@@ -109,6 +113,12 @@ cudaError_t num_sms(int *n) {
 }  // namespace tcimpl
 
 cudaError_t launch_intra_tc(const BwdArgs &a, cudaStream_t stream) {
+    if (a.factor_diag) {
+        if (a.cu_seqlens)
+            return a.fp16 ? launch_tc_fp16_varlen_fd(a, stream)
+                          : launch_tc_bf16_varlen_fd(a, stream);
+        return a.fp16 ? launch_tc_fp16_fd(a, stream) : launch_tc_bf16_fd(a, stream);
+    }
     if (a.cu_seqlens)
         return a.fp16 ? launch_tc_fp16_varlen(a, stream) : launch_tc_bf16_varlen(a, stream);
     return a.fp16 ? launch_tc_fp16(a, stream) : launch_tc_bf16(a, stream);

@@ -31,11 +31,12 @@
 //               + beta_r k[r,d] 2^(g_r - g_16j) dAkk[r,s]        (s < 16j)
 //     dkt_cross[s,d] = 2^(g_e(i) - g_s) * sum_{j>i} 2^(g_16j - g_e(i)) P_j[d, s].
 // The 16x16 diagonal blocks run on the FP32 pipes, two source rows at a time in
-// packed FP32x2 arithmetic.  Their lower-left 8x8 quadrant (rows 8..15 against
-// sources 0..7) is factorized through row 8 of the block,
+// packed FP32x2 arithmetic, with one exp2 per (r, s, d).  Optionally (FACTOR) their
+// lower-left 8x8 quadrant (rows 8..15 against sources 0..7) is factorized through
+// row 8 of the block,
 //     2^(g_r - g_s) = 2^(g_r - g_8) * 2^(g_8 - g_s),  both exponents <= 0,
-// so it costs four FMAs per (r, s, d); the two 8x8 triangles left take one exp2
-// per (r, s, d).
+// so it costs four FMAs per (r, s, d); the two 8x8 triangles keep one exp2 per
+// (r, s, d).
 #pragma once
 
 #include <cuda.h>
@@ -245,12 +246,13 @@ __device__ __forceinline__ void load_unit(unsigned char *st, uint64_t *full, int
 
 // ACCUM: add the optional incoming gradients of Extras; FOLD: return dg as its
 // inclusive reverse cumsum inside each chunk; EMIT: store dq and dk as io_t;
+// FACTOR: the diagonal blocks' lower-left quadrant through row 8 (see above);
 // VARLEN: units come from cu_seqlens / chunk_indices, and a unit's rows past its
 // sequence's end (row >= len, "foreign" rows) are masked: their q, k, beta and
 // diagonal-block dA rows read as 0, their gate as the last valid row's (so every
 // exponent stays <= 0), their off-diagonal dA rows are zeroed in the column-side
 // operands, and nothing is stored for them.
-template <typename io_t, bool ACCUM, bool FOLD, bool EMIT, bool VARLEN>
+template <typename io_t, bool ACCUM, bool FOLD, bool EMIT, bool VARLEN, bool FACTOR>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restrict__ beta,
                         void *dq_out, void *dk_out, float *db, float *dg, int T, int H,
@@ -534,11 +536,11 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         }
 
         // ---- diagonal block, two source rows at a time in packed FP32x2: one exp2 per
-        // (r, s, d), shared by both sides, in the two 8x8 triangles; the factorized
-        // quadrant in between.  Rows run in descending order: once row r is processed,
-        // its row sums and its column sum dkt[r] are complete, so each row is written
-        // out right away.  Rows 15..8 (92 of the 120 pairs, the quadrant among them) run
-        // before the MMA result is needed; rows 7..0 after it. ----
+        // (r, s, d), shared by both sides (FACTOR: in the two 8x8 triangles, with the
+        // factorized quadrant in between).  Rows run in descending order: once row r is
+        // processed, its row sums and its column sum dkt[r] are complete, so each row is
+        // written out right away.  Rows 15..8 (92 of the 120 pairs) run before the MMA
+        // result is needed; rows 7..0 after it. ----
         float accq[BC], acck[BC], dbv[BC];
         float2 dkt2[BC / 2];
 #pragma unroll
@@ -556,17 +558,19 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         const size_t obase = orow0 * KD + d;
         const uint32_t hk = (uint32_t)H * KD;
 
-        // Lower-left quadrant (rows 8..15 against sources 0..7) factorized through
-        // row 8: 2^(g_r - g_s) = 2^(g_r - g_8) 2^(g_8 - g_s), both exponents <= 0.
+        // FACTOR: the lower-left quadrant (rows 8..15 against sources 0..7) through
+        // row 8, 2^(g_r - g_s) = 2^(g_r - g_8) 2^(g_8 - g_s), both exponents <= 0.
         // kbq[m] holds k_s 2^(g_8 - g_s) for the source pair m; dktq[m] the column
         // sums still to be scaled by 2^(g_8 - g_s).
         const float g8 = KDA_EL(g2, BC / 2);
         float2 kbq[BC / 4], dktq[BC / 4];
+        if constexpr (FACTOR) {
 #pragma unroll
-        for (int m = 0; m < BC / 4; ++m) {
-            const float2 df = __ffma2_rn(g2[m], neg1, make_float2(g8, g8));
-            kbq[m] = __fmul2_rn(k2[m], make_float2(ex2(df.x), ex2(df.y)));
-            dktq[m] = make_float2(0.f, 0.f);
+            for (int m = 0; m < BC / 4; ++m) {
+                const float2 df = __ffma2_rn(g2[m], neg1, make_float2(g8, g8));
+                kbq[m] = __fmul2_rn(k2[m], make_float2(ex2(df.x), ex2(df.y)));
+                dktq[m] = make_float2(0.f, 0.f);
+            }
         }
 
         auto diag_row = [&](const int r) {
@@ -580,7 +584,7 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             // row r's 16-byte chunk c of the diagonal block sits at c*64 + roff floats
             const int roff = (r >> 3) * 32 + (r & 7) * 4;
             int cfirst = 0;
-            if (r >= BC / 2) {  // the factorized quadrant: sources 0..7
+            if (FACTOR && r >= BC / 2) {  // the factorized quadrant: sources 0..7
                 const float ar = r == BC / 2 ? 1.f : ex2(gv - g8);
                 const float2 qa = make_float2(ar * qv, ar * qv);
                 const float2 kba = make_float2(ar * kbr, ar * kbr);
@@ -706,11 +710,16 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         fetch_in(BC - 2);
         fetch_in(BC - 3);
 #pragma unroll
-        for (int r = BC - 1; r >= BC / 2; --r) diag_row(r);
+        for (int r = BC - 1; r >= BC / 2; --r) {
+            if constexpr (!FACTOR) accq[r] = acck[r] = 0.f;
+            diag_row(r);
+        }
+        if constexpr (FACTOR) {
 #pragma unroll
-        for (int m = 0; m < BC / 4; ++m) {
-            const float2 df = __ffma2_rn(g2[m], neg1, make_float2(g8, g8));
-            dkt2[m] = __ffma2_rn(make_float2(ex2(df.x), ex2(df.y)), dktq[m], dkt2[m]);
+            for (int m = 0; m < BC / 4; ++m) {
+                const float2 df = __ffma2_rn(g2[m], neg1, make_float2(g8, g8));
+                dkt2[m] = __ffma2_rn(make_float2(ex2(df.x), ex2(df.y)), dktq[m], dkt2[m]);
+            }
         }
 
         // ---- cross terms: wait for the MMAs, apply the post-factors ----
@@ -846,9 +855,9 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
 cudaError_t make_maps(const BwdArgs &a, TmaMaps *tm);
 cudaError_t num_sms(int *n);
 
-template <typename io_t, bool ACCUM, bool FOLD, bool EMIT, bool VARLEN>
+template <typename io_t, bool ACCUM, bool FOLD, bool EMIT, bool VARLEN, bool FACTOR>
 cudaError_t launch_typed(const BwdArgs &a, cudaStream_t stream) {
-    auto kern = kda_intra_bwd_tc_kernel<io_t, ACCUM, FOLD, EMIT, VARLEN>;
+    auto kern = kda_intra_bwd_tc_kernel<io_t, ACCUM, FOLD, EMIT, VARLEN, FACTOR>;
     const int smem_bytes = FOLD ? SM_TOTAL_FOLD : SM_TOTAL;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
@@ -876,21 +885,22 @@ cudaError_t launch_typed(const BwdArgs &a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-template <typename io_t, bool EMIT, bool VARLEN>
+template <typename io_t, bool EMIT, bool VARLEN, bool FACTOR>
 cudaError_t launch_opts(const BwdArgs &a, cudaStream_t stream) {
     const bool accum = a.dq_in || a.dk_in || a.dg_in || a.db_in;
     if (accum)
-        return a.fold_dg ? launch_typed<io_t, true, true, EMIT, VARLEN>(a, stream)
-                         : launch_typed<io_t, true, false, EMIT, VARLEN>(a, stream);
-    return a.fold_dg ? launch_typed<io_t, false, true, EMIT, VARLEN>(a, stream)
-                     : launch_typed<io_t, false, false, EMIT, VARLEN>(a, stream);
+        return a.fold_dg ? launch_typed<io_t, true, true, EMIT, VARLEN, FACTOR>(a, stream)
+                         : launch_typed<io_t, true, false, EMIT, VARLEN, FACTOR>(a, stream);
+    return a.fold_dg ? launch_typed<io_t, false, true, EMIT, VARLEN, FACTOR>(a, stream)
+                     : launch_typed<io_t, false, false, EMIT, VARLEN, FACTOR>(a, stream);
 }
 
-// Every option combination of one q/k element type and one sequence layout.
-template <typename io_t, bool VARLEN>
+// Every option combination of one q/k element type, one sequence layout and one
+// diagonal-block form.
+template <typename io_t, bool VARLEN, bool FACTOR>
 cudaError_t launch_io(const BwdArgs &a, cudaStream_t stream) {
-    return a.emit_io ? launch_opts<io_t, true, VARLEN>(a, stream)
-                     : launch_opts<io_t, false, VARLEN>(a, stream);
+    return a.emit_io ? launch_opts<io_t, true, VARLEN, FACTOR>(a, stream)
+                     : launch_opts<io_t, false, VARLEN, FACTOR>(a, stream);
 }
 
 }  // namespace tcimpl

@@ -1,8 +1,9 @@
-// Instantiations of the tensor-core kernel: __half q/k, variable-length sequences.
+// Instantiations of the tensor-core kernel: __half q/k, variable-length sequences,
+// one exp2 per (r, s, d) in the diagonal blocks.
 #include "kda_intra_tc.cuh"
 
 namespace kda {
 cudaError_t launch_tc_fp16_varlen(const BwdArgs &a, cudaStream_t stream) {
-    return tcimpl::launch_io<__half, true>(a, stream);
+    return tcimpl::launch_io<__half, true, false>(a, stream);
 }
 }  // namespace kda

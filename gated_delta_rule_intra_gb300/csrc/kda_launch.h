@@ -17,6 +17,7 @@ struct BwdArgs {
     const float *dq_in = nullptr, *dk_in = nullptr, *dg_in = nullptr, *db_in = nullptr;
     bool fold_dg = false;  // dg as its inclusive reverse cumsum inside each chunk
     bool emit_io = false;  // dq, dk written in the q/k element type
+    bool factor_diag = false;  // diagonal blocks' lower-left quadrant through row 8
     // variable-length sequences packed along T (B == 1): sequence n holds tokens
     // [cu_seqlens[n], cu_seqlens[n+1]); chunk c of the launch is chunk
     // chunk_indices[2c+1] of sequence chunk_indices[2c]

@@ -163,6 +163,8 @@ def test_ex_rejections(lib):
     assert ex_call(lib, H=1, HV=2, emit=1) == 9               # io-dtype outputs with GVA
     assert ex_call(lib, fold=2) == 9
     assert ex_call(lib, emit=3) == 9
+    assert ex_call(lib, ins={"factor_diag": 2}) == 9
+    assert ex_call(lib, ins={"factor_diag": -1}) == 9
     assert ex_call(lib, ins={"dq_in": BASE + 11 * SPAN + 2}) == ERR_ALIGN
     # an incoming gradient overlapping an output other than its own
     assert ex_call(lib, ins={"dk_in": BASE + 6 * SPAN}) == ERR_OVERLAP
@@ -179,6 +181,7 @@ def test_ex_accepts_in_place_and_reaches_the_device(lib):
            "dg_in": BASE + 9 * SPAN}
     assert ex_call(lib, H=2, HV=4, fold=1, ins=ins) in (ERR_CUDA, ERR_DEVICE)
     assert ex_call(lib, emit=1) in (ERR_CUDA, ERR_DEVICE)
+    assert ex_call(lib, ins={"factor_diag": 1}) in (ERR_CUDA, ERR_DEVICE)
     # NULL options behave like kda_intra_bwd
     args = fake_args()[:-1]
     assert lib.kda_intra_bwd_ex(*args, None, ctypes.c_void_p(0)) in (ERR_CUDA, ERR_DEVICE)
@@ -295,3 +298,31 @@ def test_fwd_ex_accepts_groups_and_varlen(lib):
         pytest.skip("would launch on a real device")
     assert fwd_ex_call(lib, H=2, HV=8) in (ERR_CUDA, ERR_DEVICE)
     assert fwd_ex_call(lib, T=100, ins=varlen_ins()) in (ERR_CUDA, ERR_DEVICE)
+
+
+def test_option_structs_match_the_header(tmp_path):
+    """The binding's ctypes option structs have the C header's size and field offsets
+    (compiled here with the host C compiler)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no host C compiler")
+    structs = {"kda_intra_bwd_opts_t": kda.KdaOpts, "kda_intra_fwd_opts_t": kda.KdaFwdOpts}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "kda.h"', "int main(void) {"]
+    for cname, py in structs.items():
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for field, _ in py._fields_:
+            lines.append(f'printf("{cname} {field} %zu\\n", offsetof({cname}, {field}));')
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    got = {tuple(l.split()[:2]): int(l.split()[2]) for l in out.splitlines()}
+    for cname, py in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(py), cname
+        for field, _ in py._fields_:
+            assert got[(cname, field)] == getattr(py, field).offset, (cname, field)
