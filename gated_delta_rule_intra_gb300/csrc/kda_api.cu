@@ -338,16 +338,20 @@ kda_status_t kda_intra_bwd_host(const void *q, const void *k, const float *g,
     // of piece p+1 go up on one internal stream while piece p computes on the caller's
     // stream and piece p-1 comes down on another, so both copy directions and the
     // kernel overlap.  Events order everything after earlier work on the caller's
-    // stream, and the caller's stream waits for the last copy.
+    // stream, and the caller's stream waits for the last copy.  Every copy carries a
+    // fixed cost of a few microseconds, so pieces are large (about 96 MB of input:
+    // fewer copies, against a longer pipeline fill and drain), and beta and db, 1/128
+    // of the rows' bytes, move whole: beta before the first piece, db after the last.
+    // A second copy stream per direction measured slower (the copies contend).
     const long long chunks = (long long)B * T / KDA_BT;
     const size_t in_bytes = 2 * nqk + nk4 + nrow + 2 * nda;
-    long long P = (long long)(in_bytes / ((size_t)32 << 20));
+    long long P = (long long)(in_bytes / ((size_t)96 << 20));
     if (P < 1) P = 1;
     if (P > 64) P = 64;
     if (P > chunks) P = chunks;
     cudaStream_t s = (cudaStream_t)stream, s_in = nullptr, s_out = nullptr;
-    cudaEvent_t ev[2 * 64 + 2] = {};
-    const int nev = (int)(2 * P + 2);
+    cudaEvent_t ev[2 * 64 + 4] = {};
+    const int nev = (int)(2 * P + 4);
     kda_status_t result = KDA_OK;
     auto fail = [&](kda_status_t code) {
         if (result == KDA_OK) result = code;
@@ -360,10 +364,14 @@ kda_status_t kda_intra_bwd_host(const void *q, const void *k, const float *g,
             fail(KDA_ERR_CUDA);
     const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
     if (result == KDA_OK) {
-        cudaEvent_t e_start = ev[0], e_done = ev[1];
+        cudaEvent_t e_start = ev[0], e_done = ev[1], e_beta = ev[2 * P + 2],
+                    e_last = ev[2 * P + 3];
         if (cudaEventRecord(e_start, s) != cudaSuccess ||
             cudaStreamWaitEvent(s_in, e_start, 0) != cudaSuccess ||
-            cudaStreamWaitEvent(s_out, e_start, 0) != cudaSuccess)
+            cudaStreamWaitEvent(s_out, e_start, 0) != cudaSuccess ||
+            cudaMemcpyAsync(beta_d, beta, nrow, h2d, s_in) != cudaSuccess ||
+            cudaEventRecord(e_beta, s_in) != cudaSuccess ||
+            cudaStreamWaitEvent(s, e_beta, 0) != cudaSuccess)
             fail(KDA_ERR_CUDA);
         for (long long p = 0; p < P && result == KDA_OK; ++p) {
             const long long c0 = p * chunks / P, c1 = (p + 1) * chunks / P;
@@ -372,13 +380,10 @@ kda_status_t kda_intra_bwd_host(const void *q, const void *k, const float *g,
             cudaEvent_t e_in = ev[2 + 2 * p], e_k = ev[3 + 2 * p];
             const size_t oqk = r0 * KDA_K * 2, o4 = r0 * KDA_K * 4, orow = r0 * 4,
                          oda = r0 * KDA_BT * 4;
-            const size_t lqk = nr * KDA_K * 2, l4 = nr * KDA_K * 4, lrow = nr * 4,
-                         lda = nr * KDA_BT * 4;
+            const size_t lqk = nr * KDA_K * 2, l4 = nr * KDA_K * 4, lda = nr * KDA_BT * 4;
             if (cudaMemcpyAsync(q_d + oqk, (const char *)q + oqk, lqk, h2d, s_in) != cudaSuccess ||
                 cudaMemcpyAsync(k_d + oqk, (const char *)k + oqk, lqk, h2d, s_in) != cudaSuccess ||
                 cudaMemcpyAsync(g_d + o4, (const char *)g + o4, l4, h2d, s_in) != cudaSuccess ||
-                cudaMemcpyAsync(beta_d + orow, (const char *)beta + orow, lrow, h2d, s_in) !=
-                    cudaSuccess ||
                 cudaMemcpyAsync(aqk_d + oda, (const char *)dAqk + oda, lda, h2d, s_in) !=
                     cudaSuccess ||
                 cudaMemcpyAsync(akk_d + oda, (const char *)dAkk + oda, lda, h2d, s_in) !=
@@ -401,13 +406,17 @@ kda_status_t kda_intra_bwd_host(const void *q, const void *k, const float *g,
                 cudaStreamWaitEvent(s_out, e_k, 0) != cudaSuccess ||
                 cudaMemcpyAsync((char *)dq + o4, dq_d + o4, l4, d2h, s_out) != cudaSuccess ||
                 cudaMemcpyAsync((char *)dk + o4, dk_d + o4, l4, d2h, s_out) != cudaSuccess ||
-                cudaMemcpyAsync((char *)dg + o4, dg_d + o4, l4, d2h, s_out) != cudaSuccess ||
-                cudaMemcpyAsync((char *)db + orow, db_d + orow, lrow, d2h, s_out) !=
-                    cudaSuccess) {
+                cudaMemcpyAsync((char *)dg + o4, dg_d + o4, l4, d2h, s_out) != cudaSuccess) {
                 fail(KDA_ERR_CUDA);
                 break;
             }
         }
+        // db of every piece, once the last kernel is done
+        if (result == KDA_OK &&
+            (cudaEventRecord(e_last, s) != cudaSuccess ||
+             cudaStreamWaitEvent(s_out, e_last, 0) != cudaSuccess ||
+             cudaMemcpyAsync(db, db_d, nrow, d2h, s_out) != cudaSuccess))
+            fail(KDA_ERR_CUDA);
         // the caller's stream waits for the last copy, also after a failure midway
         if (cudaEventRecord(e_done, s_out) != cudaSuccess ||
             cudaStreamWaitEvent(s, e_done, 0) != cudaSuccess)

@@ -112,7 +112,8 @@ kda_status_t kda_intra_bwd_fp32(const void *q, const void *k, const float *g,
  * into `workspace` (device memory of at least kda_intra_bwd_host_workspace_bytes()
  * bytes, caller-owned, 256-byte aligned), runs kda_intra_bwd, and copies the four
  * outputs back into the host buffers.  The work is pipelined over pieces of about
- * 32 MB of input (whole 64-token chunks): uploads run on one internal stream,
+ * 96 MB of input (whole 64-token chunks; beta goes up whole before the first piece
+ * and db comes down whole after the last): uploads run on one internal stream,
  * downloads on another and the kernels on `stream`, so both copy directions and the
  * compute overlap; events order it all after earlier work on `stream`, and `stream`
  * waits for the last download.  Copies are truly asynchronous only when the host

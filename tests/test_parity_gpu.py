@@ -167,9 +167,10 @@ def test_host_entry_point_matches_device_path():
 
 @pytest.mark.parametrize("pinned_host", [True, False])
 def test_host_entry_point_pipelined_pieces(pinned_host):
-    """About 100 MB of input: the host entry point splits it into three pieces of
-    42-43 chunks on its internal streams; the result is bitwise the device path's."""
-    B, T, H = 4, 2048, 8
+    """About 300 MB of input: the host entry point splits it into three pieces of
+    85-86 chunks on its internal streams (beta and db move whole); the result is
+    bitwise the device path's."""
+    B, T, H = 4, 4096, 12
     cpu = kda_inputs.make_inputs(B, T, H, seed=19)
     host = {n: (v.pin_memory() if pinned_host else v.clone()) for n, v in cpu.items()}
     mk = (lambda *shape: torch.empty(*shape).pin_memory()) if pinned_host else torch.empty
