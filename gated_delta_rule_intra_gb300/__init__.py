@@ -10,16 +10,20 @@ The functions carry the C names of ``include/kda.h``:
 * ``kda_intra_bwd_fp32``  -- all-FP32 path
 * ``kda_intra_bwd_ex``    -- fast path with options: grouped value heads, incoming
   gradients added in-kernel, dg folded to its chunk-local reverse cumsum, dq/dk in
-  the q/k dtype, variable-length sequences (``cu_seqlens``)
+  the q/k dtype, variable-length sequences (``cu_seqlens``), the diagonal quadrant
+  factorized (``factor_diag``)
 * ``prepare_chunk_indices`` -- the (sequence, chunk) table of a ``cu_seqlens``
 * ``kda_intra_bwd_host``  -- host buffers in and out, copies on the stream
 * ``kda_intra_fwd``       -- the forward score matrices Aqk, Akk (grouped value heads
   and variable-length sequences through ``kda_intra_fwd_ex``)
 * ``kda_status_str``, ``kda_abi_version``
+* ``use_library``, ``kda_debug_checks``, ``kda_debug_set_flags`` -- run the same calls
+  through the bounds-checked debug build ``libkda_debug.so`` (tests)
 """
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -27,6 +31,7 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkda.so")
+DEBUG_LIB_PATH = os.path.join(_HERE, "libkda_debug.so")
 
 KDA_OK = 0
 KDA_BF16 = 0
@@ -93,9 +98,43 @@ def load_library(path: str | None = None):
     lib.kda_status_str.restype = ctypes.c_char_p
     lib.kda_abi_version.argtypes = []
     lib.kda_abi_version.restype = i
+    lib.kda_debug_checks.argtypes = []
+    lib.kda_debug_checks.restype = i
+    lib.kda_debug_set_flags.argtypes = [vp]
+    lib.kda_debug_set_flags.restype = st
     if path is None:
         _lib = lib
     return lib
+
+
+@contextlib.contextmanager
+def use_library(path: str):
+    """Route every call of this module through another build of libkda (for instance
+    the bounds-checked ``libkda_debug.so``) inside the ``with`` block."""
+    global _lib
+    saved = _lib
+    _lib = load_library(path)
+    try:
+        yield _lib
+    finally:
+        _lib = saved
+
+
+def kda_debug_checks() -> bool:
+    """True when the library in use is the bounds-checked debug build."""
+    return bool(load_library().kda_debug_checks())
+
+
+def kda_debug_set_flags(word) -> None:
+    """Debug build only: later launches report index or wait failures into ``word``
+    (a CUDA int32 tensor of one element, caller-owned; None stops reporting)."""
+    if word is not None and (word.device.type != "cuda" or word.numel() != 1
+                             or word.dtype != torch.int32):
+        raise ValueError("the flag word must be a one-element int32 CUDA tensor")
+    rc = load_library().kda_debug_set_flags(
+        ctypes.c_void_p(None if word is None else word.data_ptr()))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_debug_set_flags")
 
 
 def kda_status_str(code: int) -> str:

@@ -3,6 +3,9 @@
 Each .cu under csrc/ is compiled to an object in parallel, then linked into
 ``gated_delta_rule_intra_gb300/libkda.so`` (git-ignored).  No CMake, no torch
 extension machinery: the library is a plain C-ABI shared object.
+``build_debug_library()`` builds the same sources with ``-DKDA_DEBUG_CHECKS`` into
+``libkda_debug.so``: every global index the kernels compute is checked against its
+buffer's extent and reported through ``kda_debug_set_flags`` (tests only).
 """
 
 from __future__ import annotations
@@ -17,7 +20,9 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libkda.so")
+DEBUG_LIB = os.path.join(PKG, "libkda_debug.so")
 BUILD_DIR = os.path.join(PKG, "_build")
+DEBUG_BUILD_DIR = os.path.join(PKG, "_build_debug")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -35,8 +40,8 @@ def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _compile(src: str, extra) -> str:
-    obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, extra, build_dir: str) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
     cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
@@ -44,12 +49,13 @@ def _compile(src: str, extra) -> str:
     return obj
 
 
-def build_library(out: str = LIB, extra_flags=(), verbose: bool = False) -> str:
+def build_library(out: str = LIB, extra_flags=(), verbose: bool = False,
+                  build_dir: str = BUILD_DIR) -> str:
     """Compile every csrc/*.cu for sm_103a and link libkda.so; returns its path."""
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sources()
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, list(extra_flags)), srcs))
+        objs = list(ex.map(lambda s: _compile(s, list(extra_flags), build_dir), srcs))
     tmp = out + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
@@ -61,5 +67,11 @@ def build_library(out: str = LIB, extra_flags=(), verbose: bool = False) -> str:
     return out
 
 
+def build_debug_library(verbose: bool = False) -> str:
+    """The bounds-checked debug build, libkda_debug.so; returns its path."""
+    return build_library(DEBUG_LIB, ["-DKDA_DEBUG_CHECKS"], verbose, DEBUG_BUILD_DIR)
+
+
 if __name__ == "__main__":
     build_library(verbose=True)
+    build_debug_library(verbose=True)

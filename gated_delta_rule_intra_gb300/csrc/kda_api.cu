@@ -155,6 +155,10 @@ kda_status_t check_ex(const void *q, const void *k, const float *g, const float 
     return KDA_OK;
 }
 
+// Bounds-checked debug build: the caller's device flag word (kda_debug_set_flags),
+// passed to every launch.  Always null in the normal build.
+unsigned *g_debug_flags = nullptr;
+
 kda::BwdArgs pack(const void *q, const void *k, const float *g, const float *beta,
                   const float *dAqk, const float *dAkk, float *dq, float *dk, float *db,
                   float *dg, int B, int T, int H, kda_dtype_t dt) {
@@ -163,6 +167,7 @@ kda::BwdArgs pack(const void *q, const void *k, const float *g, const float *bet
     a.dq = dq; a.dk = dk; a.db = db; a.dg = dg;
     a.B = B; a.T = T; a.H = H;
     a.fp16 = (dt == KDA_FP16);
+    a.dbg = g_debug_flags;
     return a;
 }
 
@@ -285,6 +290,7 @@ kda_status_t kda_intra_fwd_ex(const void *q, const void *k, const float *g, cons
     a.chunk_indices = o.chunk_indices;
     a.num_seqs = o.num_seqs;
     a.num_chunks = o.num_chunks;
+    a.dbg = g_debug_flags;
     return kda::launch_intra_fwd(a, (cudaStream_t)stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -450,5 +456,19 @@ const char *kda_status_str(kda_status_t status) {
 }
 
 int kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+#ifdef KDA_DEBUG_CHECKS
+int kda_debug_checks(void) { return 1; }
+
+kda_status_t kda_debug_set_flags(unsigned int *device_word) {
+    if ((uintptr_t)device_word % 4u) return KDA_ERR_ALIGN;
+    g_debug_flags = device_word;
+    return KDA_OK;
+}
+#else
+int kda_debug_checks(void) { return 0; }
+
+kda_status_t kda_debug_set_flags(unsigned int *) { return KDA_ERR_OPTION; }
+#endif
 
 }  // extern "C"

@@ -44,6 +44,27 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
+// Bounds-checked debug build (compiled with KDA_DEBUG_CHECKS): every global index a
+// kernel computes is checked against its buffer's extent before the access; an index
+// out of range sets `bit` in the caller's flag word (when one is set) and the access is
+// skipped.  In the normal build the check is the constant true and compiles away.
+constexpr unsigned DBG_STORE = 1u;  // an output index
+constexpr unsigned DBG_LOAD = 2u;   // an input index
+constexpr unsigned DBG_WAIT = 4u;   // a bounded wait gave up
+#ifdef KDA_DEBUG_CHECKS
+__device__ __forceinline__ bool dbg_ok(unsigned *flags, size_t idx, size_t n, unsigned bit) {
+    if (idx < n) return true;
+    if (flags) atomicOr(flags, bit);
+    return false;
+}
+__device__ __forceinline__ void dbg_flag(unsigned *flags, bool fail, unsigned bit) {
+    if (fail && flags) atomicOr(flags, bit);
+}
+#else
+__device__ __forceinline__ bool dbg_ok(unsigned *, size_t, size_t, unsigned) { return true; }
+__device__ __forceinline__ void dbg_flag(unsigned *, bool, unsigned) {}
+#endif
+
 // Decode a unit index into (b, h, chunk).  Heads vary fastest so that CTAs that
 // run at the same time read neighbouring addresses of the [B, T, H, *] tensors.
 struct Unit {

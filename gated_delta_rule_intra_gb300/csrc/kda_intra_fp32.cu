@@ -230,9 +230,11 @@ kda_intra_bwd_fp32_kernel(const __grid_constant__ TmaMaps tm, const float *__res
             float vq = accq[r], vk = fmaf(sbeta[row], acck[r], dkv);
             float vg = __fmul_rn(LN2, fmaf(qv, accq[r], __fmul_rn(__fsub_rn(pk, dkv), kv)));
             if (!ok) vq = vk = vg = __int_as_float(0x7fc00000);
-            dq[off] = vq;
-            dk[off] = vk;
-            dg[off] = vg;
+            if (dbg_ok(ex.dbg, off, ex.nrows * KD, DBG_STORE)) {
+                dq[off] = vq;
+                dk[off] = vk;
+                dg[off] = vg;
+            }
             dbv[r] = ok ? acck[r] * kv : __int_as_float(0x7fc00000);
         };
         // db over 8 rows: transpose-reduce across the warp's lanes (lane l ends with
@@ -271,8 +273,9 @@ kda_intra_bwd_fp32_kernel(const __grid_constant__ TmaMaps tm, const float *__res
         tc::named_bar_sync(1 + i, 128);
         if ((warp & 3) == 0 && lane < BC) {
             const int row = r0 + lane;
-            db[grow(un, row, T, H)] =
-                (dbp[row] + dbp[BT + row]) + (dbp[2 * BT + row] + dbp[3 * BT + row]);
+            const size_t bi = grow(un, row, T, H);
+            if (dbg_ok(ex.dbg, bi, ex.nrows, DBG_STORE))
+                db[bi] = (dbp[row] + dbp[BT + row]) + (dbp[2 * BT + row] + dbp[3 * BT + row]);
         }
 
         // ---- unit done: the last warp releases the stage and refills it ----
@@ -285,6 +288,7 @@ kda_intra_bwd_fp32_kernel(const __grid_constant__ TmaMaps tm, const float *__res
             load_unit<false>(st, &full[sidx], nullptr, tm, beta, u + 2 * stride, T, H, ex, lane);
         }
     }
+    dbg_flag(ex.dbg, !ok, DBG_WAIT);
 }
 
 template <typename io_t>
@@ -298,6 +302,8 @@ cudaError_t launch_typed(const BwdArgs &a, cudaStream_t stream) {
     if ((e = make_maps(a, &tm)) != cudaSuccess) return e;
     Extras ex = {};
     ex.G = 1;
+    ex.dbg = a.dbg;
+    ex.nrows = (size_t)a.B * a.T * a.H;
     const long long units = (long long)a.B * a.H * (a.T / BT);
     const unsigned grid = (unsigned)(units < nsm ? units : nsm);
     kern<<<grid, TC_THREADS, F_TOTAL, stream>>>(tm, a.beta, (float *)a.dq, (float *)a.dk, a.db,

@@ -88,6 +88,10 @@ struct FwdExtras {
     int G;
     const int *cu_seqlens, *chunk_indices;
     int num_seqs;
+    // bounds-checked debug build: the flag word and the extents checked against
+    unsigned *dbg;
+    size_t nrows;    // token rows x heads of g, beta and the outputs
+    int num_chunks;  // entries of chunk_indices (variable-length launches)
 };
 
 // First token row and valid rows (1..64) of a variable-length unit; {0, 0} for an
@@ -95,9 +99,10 @@ struct FwdExtras {
 __device__ __forceinline__ void varlen_rows(long long u, int H, int T, const FwdExtras &ex,
                                             int &start, int &len) {
     const size_t c = (size_t)((unsigned)u / (unsigned)H);
-    const int n = __ldg(ex.chunk_indices + 2 * c), j = __ldg(ex.chunk_indices + 2 * c + 1);
     start = 0;
     len = 0;
+    if (!dbg_ok(ex.dbg, 2 * c + 1, 2 * (size_t)ex.num_chunks, DBG_LOAD)) return;
+    const int n = __ldg(ex.chunk_indices + 2 * c), j = __ldg(ex.chunk_indices + 2 * c + 1);
     if (n >= 0 && n < ex.num_seqs && j >= 0) {
         const long long bos = __ldg(ex.cu_seqlens + n), eos = __ldg(ex.cu_seqlens + n + 1);
         const long long st = bos + (long long)BT * j;
@@ -143,7 +148,7 @@ __device__ __forceinline__ void load_unit(unsigned char *st, float *sbeta, uint6
     for (int e = 0; e < 2; ++e) {
         const int r = lane + 32 * e;
         const uint32_t s = tc::smem_u32(sbeta + r);
-        const bool take = r < len;
+        const bool take = r < len && dbg_ok(ex.dbg, (size_t)(row + r) * H + h, ex.nrows, DBG_LOAD);
         asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(s),
                      "l"(take ? b0 + (size_t)r * H : beta), "r"(take ? 4 : 0)
                      : "memory");
@@ -516,8 +521,9 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
                 const int tensor = x >= per, rem = x - tensor * per;
                 const int r = rem / (BT / 4), c4 = rem % (BT / 4);
                 const float4 v = *reinterpret_cast<const float4 *>(stg + stg_off(tensor, r, 4 * c4));
-                float *dst = (tensor ? Akk : Aqk) + ((size_t)(row + r) * H + h) * BT + 4 * c4;
-                *reinterpret_cast<float4 *>(dst) = v;
+                const size_t di = ((size_t)(row + r) * H + h) * BT + 4 * c4;
+                if (dbg_ok(ex.dbg, di + 3, ex.nrows * BT, DBG_STORE))
+                    *reinterpret_cast<float4 *>((tensor ? Akk : Aqk) + di) = v;
             }
             __syncthreads();  // the staging is read before the next unit may write it
         }
@@ -527,6 +533,7 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
                                     H, ex, lane);
     }
 
+    dbg_flag(ex.dbg, !ok, DBG_WAIT);
     if (tid == 0) tc::bulk_wait_all();
     tc::fence_before_sync();
     __syncthreads();
@@ -598,6 +605,9 @@ cudaError_t launch_typed(const FwdArgs &a, cudaStream_t stream) {
     ex.cu_seqlens = a.cu_seqlens;
     ex.chunk_indices = a.chunk_indices;
     ex.num_seqs = a.num_seqs;
+    ex.dbg = a.dbg;
+    ex.nrows = (size_t)a.B * a.T * HV;
+    ex.num_chunks = a.num_chunks;
     const long long units =
         VARLEN ? (long long)a.num_chunks * HV : (long long)a.B * HV * (a.T / BT);
     if (units == 0) return cudaSuccess;

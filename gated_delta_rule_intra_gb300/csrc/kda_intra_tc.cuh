@@ -120,6 +120,10 @@ struct Extras {
     // sequence chunk_indices[2c], c = u / H
     const int *cu_seqlens, *chunk_indices;
     int num_seqs;
+    // bounds-checked debug build: the flag word and the extents checked against
+    unsigned *dbg;
+    size_t nrows;    // token rows x heads of g, beta, dA and the outputs
+    int num_chunks;  // entries of chunk_indices (variable-length launches)
 };
 
 // Where a variable-length unit lives: first token row, valid rows (1..64; 0 for an
@@ -135,6 +139,7 @@ __device__ __forceinline__ VarUnit varlen_unit(long long u, int H, int T, const 
     x.h = (int)(uu - c * (unsigned)H);
     x.start = 0;
     x.len = 0;
+    if (!dbg_ok(ex.dbg, 2 * (size_t)c + 1, 2 * (size_t)ex.num_chunks, DBG_LOAD)) return x;
     const int n = __ldg(ex.chunk_indices + 2 * (size_t)c);
     const int ci = __ldg(ex.chunk_indices + 2 * (size_t)c + 1);
     if (n >= 0 && n < ex.num_seqs && ci >= 0) {
@@ -236,10 +241,16 @@ __device__ __forceinline__ void load_unit(unsigned char *st, uint64_t *full, int
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
         const int r = lane + 32 * e;
-        if constexpr (VARLEN)
-            cp_async4_zfill(st + ST_BETA + r * 4, r < len ? b0 + (size_t)r * H : beta, r < len);
-        else
-            cp_async4(st + ST_BETA + r * 4, b0 + (size_t)r * H);
+        const size_t bi = (size_t)(row + r) * H + h;
+        if constexpr (VARLEN) {
+            const bool take = r < len && dbg_ok(ex.dbg, bi, ex.nrows, DBG_LOAD);
+            cp_async4_zfill(st + ST_BETA + r * 4, take ? b0 + (size_t)r * H : beta, take);
+        } else {
+            if (dbg_ok(ex.dbg, bi, ex.nrows, DBG_LOAD))
+                cp_async4(st + ST_BETA + r * 4, b0 + (size_t)r * H);
+            else
+                cp_async4_zfill(st + ST_BETA + r * 4, beta, false);
+        }
     }
     tc::cp_async_mbar_arrive_noinc(full);
 }
@@ -355,8 +366,12 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         const bool vlead = VARLEN && tid == 0 && u + 2 * stride < units;
         if (vlead) {
             const size_t c = (size_t)((unsigned)(u + 2 * stride) / (unsigned)H);
-            cp_async4(vpipe, ex.chunk_indices + 2 * c);
-            cp_async4(vpipe + 1, ex.chunk_indices + 2 * c + 1);
+            if (dbg_ok(ex.dbg, 2 * c + 1, 2 * (size_t)ex.num_chunks, DBG_LOAD)) {
+                cp_async4(vpipe, ex.chunk_indices + 2 * c);
+                cp_async4(vpipe + 1, ex.chunk_indices + 2 * c + 1);
+            } else {  // (debug build only) an entry that names nothing
+                vpipe[0] = vpipe[1] = -1;
+            }
             cp_async_commit();
         }
 
@@ -644,9 +659,10 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             if constexpr (ACCUM) {
                 const bool live = !VARLEN || r0 + r < ulen;
                 const size_t off = obase + (size_t)((uint32_t)r * hk);
-                inq[r] = (live && ex.dq_in) ? __ldg(ex.dq_in + off) : 0.f;
-                ink[r] = (live && ex.dk_in) ? __ldg(ex.dk_in + off) : 0.f;
-                ing[r] = (live && ex.dg_in) ? __ldg(ex.dg_in + off) : 0.f;
+                const bool rd = live && dbg_ok(ex.dbg, off, ex.nrows * KD, DBG_LOAD);
+                inq[r] = (rd && ex.dq_in) ? __ldg(ex.dq_in + off) : 0.f;
+                ink[r] = (rd && ex.dk_in) ? __ldg(ex.dk_in + off) : 0.f;
+                ing[r] = (rd && ex.dg_in) ? __ldg(ex.dg_in + off) : 0.f;
             }
         };
         float fold_run = 0.f;  // FOLD: running suffix sum of dg inside the sub-block
@@ -655,7 +671,8 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             const int row = r0 + r;
             const size_t off = obase + (size_t)((uint32_t)r * hk);
             if (r >= 3) fetch_in(r - 3);
-            const bool live = !VARLEN || row < ulen;  // foreign rows: nothing is stored
+            // foreign rows: nothing is stored
+            const bool live = (!VARLEN || row < ulen) && dbg_ok(ex.dbg, off, ex.nrows * KD, DBG_STORE);
             const float qv = to_f32(sq[row * KD + d]);
             const float kv = KDA_EL(k2, r), dkv = KDA_EL(dkt2, r);
             // every rounding spelled out (no compiler-chosen contraction), so all
@@ -806,10 +823,12 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
                 VARLEN ? (size_t)(meta[2 * sidx] + row) * H + (int)((unsigned)u % (unsigned)H)
                        : grow(decode_unit(u, H, NT), row, T, H);
             float v = (sdbp[row] + sdbp[BT + row]) + (sdbp[2 * BT + row] + sdbp[3 * BT + row]);
-            if constexpr (ACCUM) {
-                if (ex.db_in) v += ex.db_in[brow];
+            if (dbg_ok(ex.dbg, brow, ex.nrows, DBG_STORE)) {
+                if constexpr (ACCUM) {
+                    if (ex.db_in) v += ex.db_in[brow];
+                }
+                db[brow] = v;
             }
-            db[brow] = v;
         }
         if constexpr (FOLD) {
             // the four threads of channel d (one per sub-block, in warps c, c+4, c+8,
@@ -823,9 +842,11 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             for (int j = NBLK - 1; j > 0; --j)
                 if (j > i) later += tot[j * KD + d];
 #pragma unroll
-            for (int r = 0; r < BC; ++r)
-                if (!VARLEN || r0 + r < ulen)
-                    dg[obase + (size_t)((uint32_t)r * hk)] = bank[(r0 + r) * KD + d] + later;
+            for (int r = 0; r < BC; ++r) {
+                const size_t off = obase + (size_t)((uint32_t)r * hk);
+                if ((!VARLEN || r0 + r < ulen) && dbg_ok(ex.dbg, off, ex.nrows * KD, DBG_STORE))
+                    dg[off] = bank[(r0 + r) * KD + d] + later;
+            }
         }
 
         // ---- unit done: the last warp releases the stage and refills it ----
@@ -841,6 +862,7 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         }
     }
 
+    dbg_flag(ex.dbg, !ok, DBG_WAIT);
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) {
@@ -876,6 +898,9 @@ cudaError_t launch_typed(const BwdArgs &a, cudaStream_t stream) {
     ex.cu_seqlens = a.cu_seqlens;
     ex.chunk_indices = a.chunk_indices;
     ex.num_seqs = a.num_seqs;
+    ex.dbg = a.dbg;
+    ex.nrows = (size_t)a.B * a.T * HV;
+    ex.num_chunks = a.num_chunks;
     const long long units =
         VARLEN ? (long long)a.num_chunks * HV : (long long)a.B * HV * (a.T / BT);
     if (units == 0) return cudaSuccess;

@@ -18,6 +18,7 @@ struct BwdArgs {
     bool fold_dg = false;  // dg as its inclusive reverse cumsum inside each chunk
     bool emit_io = false;  // dq, dk written in the q/k element type
     bool factor_diag = false;  // diagonal blocks' lower-left quadrant through row 8
+    unsigned *dbg = nullptr;   // bounds-checked debug build: the caller's flag word
     // variable-length sequences packed along T (B == 1): sequence n holds tokens
     // [cu_seqlens[n], cu_seqlens[n+1]); chunk c of the launch is chunk
     // chunk_indices[2c+1] of sequence chunk_indices[2c]
@@ -36,12 +37,13 @@ struct FwdArgs {
     // variable-length sequences, as in BwdArgs
     const int *cu_seqlens = nullptr, *chunk_indices = nullptr;
     int num_seqs = 0, num_chunks = 0;
+    unsigned *dbg = nullptr;  // bounds-checked debug build: the caller's flag word
 };
 
 // Tensor-core (tcgen05 TF32) forward kernel.
 cudaError_t launch_intra_fwd(const FwdArgs &a, cudaStream_t stream);
 
-// All-FP32 SIMT kernel (one CTA per unit).
+// All-FP32 SIMT kernel (persistent, one CTA per SM).
 cudaError_t launch_intra_fp32(const BwdArgs &a, cudaStream_t stream);
 
 // Tensor-core (tcgen05 TF32) kernel.

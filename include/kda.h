@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 6
+#define KDA_ABI_VERSION 7
 #define KDA_BT 64  /* chunk length */
 #define KDA_BC 16  /* sub-block length inside a chunk */
 #define KDA_K 128  /* head dimension */
@@ -78,7 +78,8 @@ typedef enum {
     KDA_ERR_UNSUPPORTED_DEVICE = 6, /* current device is not compute capability 10.3 */
     KDA_ERR_OVERLAP = 7,            /* two argument buffers overlap */
     KDA_ERR_WORKSPACE = 8,          /* workspace missing or too small (*_host only) */
-    KDA_ERR_OPTION = 9              /* unsupported option combination (*_ex only) */
+    KDA_ERR_OPTION = 9              /* unsupported option combination (*_ex), or debug
+                                       reporting asked of a build without checks */
 } kda_status_t;
 
 typedef enum { KDA_BF16 = 0, KDA_FP16 = 1 } kda_dtype_t;
@@ -245,6 +246,27 @@ kda_status_t kda_intra_fwd_ex(const void *q, const void *k, const float *g,
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *kda_status_str(kda_status_t status);
+
+/*
+ * Bounds-checked debug build.  The same sources compiled with -DKDA_DEBUG_CHECKS (the
+ * build script's libkda_debug.so) check every global index their kernels compute
+ * (output stores, incoming-gradient and beta reads, chunk-table reads) against the
+ * extent of its buffer.  An index out of range sets KDA_DBG_STORE or KDA_DBG_LOAD in a
+ * caller-owned device word and the access is skipped; a bounded wait that gives up sets
+ * KDA_DBG_WAIT.  Nothing traps or asserts.  TMA tiles need no check: the tensor maps
+ * clip them.
+ *
+ * kda_debug_checks() is 1 in such a build, 0 otherwise.  kda_debug_set_flags(word)
+ * makes every later launch of this library report into `word` (device memory, 4 bytes,
+ * caller-owned; NULL stops reporting); the library never clears or reads it.  Set it
+ * before launching, from one thread.  Returns KDA_ERR_OPTION in a build without checks
+ * and KDA_ERR_ALIGN for a word that is not 4-byte aligned.
+ */
+#define KDA_DBG_STORE 1u
+#define KDA_DBG_LOAD 2u
+#define KDA_DBG_WAIT 4u
+int kda_debug_checks(void);
+kda_status_t kda_debug_set_flags(unsigned int *device_word);
 
 /* KDA_ABI_VERSION of the loaded library. */
 int kda_abi_version(void);

@@ -32,13 +32,20 @@ def pytest_collection_modifyitems(config, items):
 
 @pytest.fixture(scope="session", autouse=True)
 def _built_library():
-    """Build libkda.so in-tree if it is missing or older than its sources."""
+    """Build libkda.so and its bounds-checked debug build in-tree if either is missing
+    or older than its sources."""
+    import concurrent.futures
     import glob
 
     from gated_delta_rule_intra_gb300 import build
     srcs = glob.glob(os.path.join(build.CSRC, "*")) + glob.glob(
         os.path.join(ROOT, "include", "*.h"))
-    if (not os.path.exists(build.LIB)
-            or os.path.getmtime(build.LIB) < max(os.path.getmtime(s) for s in srcs)):
-        build.build_library()
+    newest = max(os.path.getmtime(s) for s in srcs)
+    jobs = [fn for path, fn in ((build.LIB, build.build_library),
+                                (build.DEBUG_LIB, build.build_debug_library))
+            if not os.path.exists(path) or os.path.getmtime(path) < newest]
+    if jobs:
+        with concurrent.futures.ThreadPoolExecutor(len(jobs)) as ex:
+            for f in [ex.submit(fn) for fn in jobs]:
+                f.result()
     yield

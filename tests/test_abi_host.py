@@ -326,3 +326,21 @@ def test_option_structs_match_the_header(tmp_path):
         assert got[(cname, "size")] == ctypes.sizeof(py), cname
         for field, _ in py._fields_:
             assert got[(cname, field)] == getattr(py, field).offset, (cname, field)
+
+
+def test_release_build_has_no_debug_checks(lib):
+    assert lib.kda_debug_checks() == 0
+    assert lib.kda_debug_set_flags(None) == 9  # KDA_ERR_OPTION
+
+
+def test_debug_build_loads_and_takes_a_flag_word():
+    dbg = kda.load_library(kda.DEBUG_LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(dbg, name), f"libkda_debug.so does not export {name}"
+    assert dbg.kda_debug_checks() == 1
+    assert dbg.kda_abi_version() == kda.kda_abi_version()
+    assert dbg.kda_debug_set_flags(ctypes.c_void_p(BASE + 2)) == ERR_ALIGN
+    assert dbg.kda_debug_set_flags(None) == OK
+    # the same argument checks as the release build
+    assert ex_call(dbg, H=2, HV=3) == ERR_SHAPE
+    assert ex_call(dbg, ins={"factor_diag": 2}) == 9
