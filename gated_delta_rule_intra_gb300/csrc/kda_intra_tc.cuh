@@ -357,6 +357,24 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             tc::named_bar_sync(9 + i, 128);
         }
 
+        // ACCUM: the unit's incoming-gradient rows (3 tensors x 64 rows of 512 bytes) are
+        // requested into L2 now; the epilogue reads them a few microseconds later
+        if constexpr (ACCUM) {
+            if (tid < 3 * BT) {
+                const int tsel = tid / BT, r = tid % BT;
+                const float *src = tsel == 0 ? ex.dq_in : tsel == 1 ? ex.dk_in : ex.dg_in;
+                size_t grow0;
+                if constexpr (VARLEN) {
+                    grow0 = (size_t)meta[2 * sidx] * H + (int)((unsigned)u % (unsigned)H);
+                } else {
+                    grow0 = grow(decode_unit(u, H, NT), 0, T, H);
+                }
+                const size_t gi = (grow0 + (size_t)r * H) * KD;
+                if (src && r < ulen && dbg_ok(ex.dbg, gi + KD - 1, ex.nrows * KD, DBG_LOAD))
+                    tc::prefetch_l2(src + gi, KD * 4);
+            }
+        }
+
         // VARLEN: thread 0 looks up the row range of the unit after next in three
         // steps spread over this unit (chunk-table entry, then the sequence's bounds,
         // then the range), all through cp.async into shared memory, so no warp ever
