@@ -49,7 +49,9 @@ constexpr int FM_BAR = FM_DIAG + 2 * 512 * 4;   // full[2], mma, staging free
 constexpr int FM_CNT = FM_BAR + 32;             // operand counter
 constexpr int FM_TSLOT = FM_CNT + 8;
 constexpr int FM_META = FM_TSLOT + 8;           // varlen: per stage {first token row, valid rows}
-constexpr int FM_TOTAL = FM_META + 16;
+constexpr int FM_LUT = FM_META + 16;            // varlen: the same for this CTA's units,
+constexpr int LUT_BATCH = 32;                   // two batches of 32
+constexpr int FM_TOTAL = FM_LUT + 2 * LUT_BATCH * 8;
 constexpr int FM_ALLOC = FM_TOTAL + 1024;       // slack for aligning the base
 static_assert(FM_STG % 1024 == 0, "swizzled staging needs 1024-byte alignment");
 static_assert(FM_ALLOC <= 232448, "shared memory");
@@ -116,15 +118,22 @@ __device__ __forceinline__ void varlen_rows(long long u, int H, int T, const Fwd
 // One warp queues a unit's copies: 8 swizzled TMA boxes from lane 0 (rows past the
 // tensor's end are zero-filled), beta as 64 four-byte cp.async copies from all lanes
 // (zero-filled past the unit's valid rows).  A variable-length unit's row range is
-// recorded in `meta` by lane 0 before its arrival on the stage barrier.
+// recorded in `meta` by lane 0 before its arrival on the stage barrier; it comes from
+// `known` ({first row, valid rows}) when given, else from the chunk table.
 template <typename io_t, bool VARLEN>
 __device__ __forceinline__ void load_unit(unsigned char *st, float *sbeta, uint64_t *full,
                                           int *meta, const FwdMaps &tm,
                                           const float *__restrict__ beta, long long u, int T,
-                                          int H, const FwdExtras &ex, int lane) {
+                                          int H, const FwdExtras &ex, int lane,
+                                          const int *known = nullptr) {
     int row, h, len = BT;
     if constexpr (VARLEN) {
-        varlen_rows(u, H, T, ex, row, len);
+        if (known) {
+            row = known[0];
+            len = known[1];
+        } else {
+            varlen_rows(u, H, T, ex, row, len);
+        }
         h = (int)((unsigned)u % (unsigned)H);
         if (lane == 0) {
             meta[0] = row;
@@ -235,6 +244,20 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
     tc::fence_after_sync();
     const uint32_t tbase = *tslot;
 
+    // VARLEN: lane j of warp 0 looks up the row range of this CTA's unit k0 + j, for the
+    // refills of a whole batch of units at once (warp 0 also does every refill)
+    int *lut = reinterpret_cast<int *>(smem + FM_LUT);
+    auto lookup_batch = [&](const int k0) {
+        const long long uk = blockIdx.x + (long long)(k0 + lane) * stride;
+        if (uk < units) {
+            int start, len;
+            varlen_rows(uk, H, T, ex, start, len);
+            int *e = lut + ((k0 / LUT_BATCH) & 1) * 2 * LUT_BATCH + 2 * lane;
+            e[0] = start;
+            e[1] = len;
+        }
+        __syncwarp();
+    };
     if (warp == 0) {
         const long long u0 = blockIdx.x;
         float *sb = reinterpret_cast<float *>(smem + FM_BETA);
@@ -243,6 +266,10 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
         if (u0 + stride < units)
             load_unit<io_t, VARLEN>(smem + FSTAGE, sb + 64, &full[1], meta + 2, tm, beta,
                                     u0 + stride, T, H, ex, lane);
+        if constexpr (VARLEN) {
+            lookup_batch(0);
+            lookup_batch(LUT_BATCH);
+        }
     }
 
     const float nan = __int_as_float(0x7fc00000);
@@ -527,10 +554,16 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
             }
             __syncthreads();  // the staging is read before the next unit may write it
         }
+        if constexpr (VARLEN) {
+            if (warp == 0 && ((it + 2) % LUT_BATCH) == 0) lookup_batch(it + 2 + LUT_BATCH);
+        }
         if (warp == 0 && u + 2 * stride < units)
             load_unit<io_t, VARLEN>(st, reinterpret_cast<float *>(smem + FM_BETA) + 64 * sidx,
                                     &full[sidx], meta + 2 * sidx, tm, beta, u + 2 * stride, T,
-                                    H, ex, lane);
+                                    H, ex, lane,
+                                    VARLEN ? lut + (((it + 2) / LUT_BATCH) & 1) * 2 * LUT_BATCH +
+                                                 2 * ((it + 2) % LUT_BATCH)
+                                           : nullptr);
     }
 
     dbg_flag(ex.dbg, !ok, DBG_WAIT);

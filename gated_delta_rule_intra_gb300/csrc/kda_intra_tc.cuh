@@ -74,9 +74,10 @@ constexpr int SM_MMA = SM_FULL + 16;         // MMAs-done mbarrier
 constexpr int SM_CNT = SM_MMA + 8;           // operand counter, unit-done counter
 constexpr int SM_TSLOT = SM_CNT + 8;
 constexpr int SM_META = SM_TSLOT + 8;        // varlen: per stage {first token row, valid rows}
-constexpr int SM_PEND = SM_META + 16;        // varlen: the same for the unit after next
-constexpr int SM_VPIPE = SM_PEND + 16;       // varlen: chunk-table lookup in flight
-constexpr int SM_TOTAL = SM_VPIPE + 16;
+constexpr int SM_LUT = SM_META + 16;         // varlen: {first row, valid rows} of this
+                                             // CTA's units, two batches of 32
+constexpr int LUT_BATCH = 32;
+constexpr int SM_TOTAL = SM_LUT + 2 * LUT_BATCH * 8;
 // extra shared memory of the fold_dg variant: the per-row dg bank [64][128] and the
 // per-(sub-block, channel) totals, double-buffered by unit parity
 constexpr int SM_FOLD_BANK = (SM_TOTAL + 127) / 128 * 128;
@@ -305,12 +306,25 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
     const uint32_t tlane = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
 
     int *meta = reinterpret_cast<int *>(smem + SM_META);
+    int *lut = reinterpret_cast<int *>(smem + SM_LUT);
+    // VARLEN: lane j of warp 0 looks up the row range of this CTA's unit k0 + j (two
+    // dependent table reads), for the refills of a whole batch of units at once
+    auto lookup_batch = [&](const int k0) {
+        const long long uk = blockIdx.x + (long long)(k0 + lane) * stride;
+        if (uk < units) {
+            const VarUnit x = varlen_unit(uk, H, T, ex);
+            int *e = lut + ((k0 / LUT_BATCH) & 1) * 2 * LUT_BATCH + 2 * lane;
+            e[0] = x.start;
+            e[1] = x.len;
+        }
+    };
     if (warp == 0) {  // the first two units of this CTA
         const long long u0 = blockIdx.x;
         if (u0 < units) load_unit<VARLEN>(smem, &full[0], meta, tm, beta, u0, T, H, ex, lane);
         if (u0 + stride < units)
             load_unit<VARLEN>(smem + STAGE_BYTES, &full[1], meta + 2, tm, beta, u0 + stride, T,
                               H, ex, lane);
+        if constexpr (VARLEN) lookup_batch(0);
     }
 
     bool ok = true;
@@ -375,22 +389,10 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             }
         }
 
-        // VARLEN: thread 0 looks up the row range of the unit after next in three
-        // steps spread over this unit (chunk-table entry, then the sequence's bounds,
-        // then the range), all through cp.async into shared memory, so no warp ever
-        // waits on a dependent global load; the refill reads the result.
-        int *vpipe = reinterpret_cast<int *>(smem + SM_VPIPE);
-        int *pend = reinterpret_cast<int *>(smem + SM_PEND) + 2 * sidx;
-        const bool vlead = VARLEN && tid == 0 && u + 2 * stride < units;
-        if (vlead) {
-            const size_t c = (size_t)((unsigned)(u + 2 * stride) / (unsigned)H);
-            if (dbg_ok(ex.dbg, 2 * c + 1, 2 * (size_t)ex.num_chunks, DBG_LOAD)) {
-                cp_async4(vpipe, ex.chunk_indices + 2 * c);
-                cp_async4(vpipe + 1, ex.chunk_indices + 2 * c + 1);
-            } else {  // (debug build only) an entry that names nothing
-                vpipe[0] = vpipe[1] = -1;
-            }
-            cp_async_commit();
+        // VARLEN: once every 32 units, warp 0 looks up the next batch; the refills read
+        // the batch table (published by warp 0's unit-done arrivals)
+        if constexpr (VARLEN) {
+            if (warp == 0 && (it % LUT_BATCH) == 0) lookup_batch(it + LUT_BATCH);
         }
 
         // ---- column-side B operands: dA blocks (j, 0..j-1) transposed.  The loads go
@@ -557,16 +559,6 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             }
         }
         __syncwarp();
-        if (vlead) {  // lookup step 2: the sequence's bounds (an entry naming no sequence
-                      // is marked with chunk -1 and reads nothing)
-            cp_async_wait_all();
-            const int n = vpipe[0], j = vpipe[1];
-            const bool named = n >= 0 && n < ex.num_seqs && j >= 0;
-            if (!named) vpipe[1] = -1;
-            cp_async4_zfill(vpipe + 2, named ? ex.cu_seqlens + n : ex.cu_seqlens, named);
-            cp_async4_zfill(vpipe + 3, named ? ex.cu_seqlens + n + 1 : ex.cu_seqlens, named);
-            cp_async_commit();
-        }
 
         // ---- diagonal block, two source rows at a time in packed FP32x2: one exp2 per
         // (r, s, d), shared by both sides (FACTOR: in the two 8x8 triangles, with the
@@ -760,22 +752,6 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         // ---- cross terms: wait for the MMAs, apply the post-factors ----
         ok &= tc::mbar_wait(mbar, (uint32_t)it & 1u, SPIN_LIMIT);
         tc::fence_after_sync();
-        if (vlead) {  // lookup step 3: the row range, published by warp 0's unit-done
-                      // arrival below
-            cp_async_wait_all();
-            const long long bos = vpipe[2], eos = vpipe[3];
-            const int j = vpipe[1];
-            int start = 0, len = 0;
-            if (j >= 0) {
-                const long long st0 = bos + (long long)BT * j;
-                if (bos >= 0 && st0 < eos && eos <= T) {
-                    start = (int)st0;
-                    len = (int)(eos - st0 < BT ? eos - st0 : BT);
-                }
-            }
-            pend[0] = start;
-            pend[1] = len;
-        }
         if (i > 0) {
             float f[BC], x[BC];
             tc::tmem_ld16(tlane + TM_FB + 16 * (i - 1), f);
@@ -876,7 +852,9 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         if ((prev % TC_WARPS) == TC_WARPS - 1 && u + 2 * stride < units) {
             tc::fence_proxy_async_smem();
             load_unit<VARLEN>(st, &full[sidx], meta + 2 * sidx, tm, beta, u + 2 * stride, T, H,
-                              ex, lane, pend);
+                              ex, lane,
+                              lut + (((it + 2) / LUT_BATCH) & 1) * 2 * LUT_BATCH +
+                                  2 * ((it + 2) % LUT_BATCH));
         }
     }
 
