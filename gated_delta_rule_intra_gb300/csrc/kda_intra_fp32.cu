@@ -44,7 +44,6 @@ kda_intra_bwd_fp32_kernel(const __grid_constant__ TmaMaps tm, const float *__res
     const int i = tid >> 7;  // sub-block, warp-uniform
     const int d = tid & 127;
     const int r0 = i * BC;
-    const int NT = T / BT;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + F_FULL);
     uint32_t *done_count = reinterpret_cast<uint32_t *>(smem + F_CNT);
     float *sdbp = reinterpret_cast<float *>(smem + F_DBP);
@@ -71,7 +70,12 @@ kda_intra_bwd_fp32_kernel(const __grid_constant__ TmaMaps tm, const float *__res
 
     bool ok = true;
     int it = 0;
-    for (long long u = blockIdx.x; u < units; u += stride, ++it) {
+    // head of the current unit, advanced by stride mod H; u = q H + h makes the unit's
+    // first [token * H + head] row 64 u - 63 h, with no division per unit
+    const unsigned dhh = (unsigned)stride % (unsigned)H;
+    unsigned hh = (unsigned)blockIdx.x % (unsigned)H;
+    for (long long u = blockIdx.x; u < units;
+         u += stride, ++it, hh = hh + dhh >= (unsigned)H ? hh + dhh - (unsigned)H : hh + dhh) {
         const int sidx = it & 1;
         unsigned char *st = smem + sidx * STAGE_BYTES;
         ok &= tc::mbar_wait(&full[sidx], (uint32_t)(it >> 1) & 1u, SPIN_LIMIT);
@@ -178,8 +182,8 @@ kda_intra_bwd_fp32_kernel(const __grid_constant__ TmaMaps tm, const float *__res
         const float *dgq = daq + dablk(i, i) * 256;
         const float *dgk = dak + dablk(i, i) * 256;
         const float2 neg1 = make_float2(-1.f, -1.f);
-        const Unit un = decode_unit(u, H, NT);
-        const size_t obase = grow(un, r0, T, H) * KD + d;
+        const size_t urow0 = (size_t)64 * (size_t)u - (size_t)63 * hh;
+        const size_t obase = (urow0 + (size_t)r0 * H) * KD + d;
         const uint32_t hk = (uint32_t)H * KD;
         float dbv[BC];
         auto diag_row = [&](const int r) {
@@ -273,7 +277,7 @@ kda_intra_bwd_fp32_kernel(const __grid_constant__ TmaMaps tm, const float *__res
         tc::named_bar_sync(1 + i, 128);
         if ((warp & 3) == 0 && lane < BC) {
             const int row = r0 + lane;
-            const size_t bi = grow(un, row, T, H);
+            const size_t bi = urow0 + (size_t)row * H;
             if (dbg_ok(ex.dbg, bi, ex.nrows, DBG_STORE))
                 db[bi] = (dbp[row] + dbp[BT + row]) + (dbp[2 * BT + row] + dbp[3 * BT + row]);
         }

@@ -277,7 +277,6 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
     const int i = tid >> 7;  // sub-block, warp-uniform
     const int d = tid & 127;
     const int r0 = i * BC;
-    const int NT = T / BT;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM_FULL);
     uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + SM_MMA);
     uint32_t *ops_count = reinterpret_cast<uint32_t *>(smem + SM_CNT);
@@ -329,7 +328,21 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
 
     bool ok = true;
     int it = 0;
-    for (long long u = blockIdx.x; u < units; u += stride, ++it) {
+    // Head of the current unit, advanced by stride mod H each iteration.  With u = q H + h
+    // the unit's first [token * H + head] row is 64 u - 63 h, so no unit needs a division.
+    // (The incoming-gradient variant keeps the decode: its registers are fuller.)
+    const unsigned dhh = (unsigned)stride % (unsigned)H;
+    unsigned hh = (unsigned)blockIdx.x % (unsigned)H;
+    auto unit_row = [&](const long long u, const int r) -> size_t {  // fixed-length: row r
+        if constexpr (ACCUM) return grow(decode_unit(u, H, T / BT), r, T, H);
+        else return (size_t)64 * (size_t)u - (size_t)63 * hh + (size_t)r * H;
+    };
+    auto unit_head = [&](const long long u) -> unsigned {
+        if constexpr (ACCUM) return (unsigned)u % (unsigned)H;
+        else return hh;
+    };
+    for (long long u = blockIdx.x; u < units;
+         u += stride, ++it, hh = hh + dhh >= (unsigned)H ? hh + dhh - (unsigned)H : hh + dhh) {
         const int sidx = it & 1;
         unsigned char *st = smem + sidx * STAGE_BYTES;
         ok &= tc::mbar_wait(&full[sidx], (uint32_t)(it >> 1) & 1u, SPIN_LIMIT);
@@ -379,9 +392,9 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
                 const float *src = tsel == 0 ? ex.dq_in : tsel == 1 ? ex.dk_in : ex.dg_in;
                 size_t grow0;
                 if constexpr (VARLEN) {
-                    grow0 = (size_t)meta[2 * sidx] * H + (int)((unsigned)u % (unsigned)H);
+                    grow0 = (size_t)meta[2 * sidx] * H + unit_head(u);
                 } else {
-                    grow0 = grow(decode_unit(u, H, NT), 0, T, H);
+                    grow0 = unit_row(u, 0);
                 }
                 const size_t gi = (grow0 + (size_t)r * H) * KD;
                 if (src && r < ulen && dbg_ok(ex.dbg, gi + KD - 1, ex.nrows * KD, DBG_LOAD))
@@ -575,10 +588,9 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         const float2 neg1 = make_float2(-1.f, -1.f);
         size_t orow0;  // output row (token * H + head) of row r0
         if constexpr (VARLEN) {
-            orow0 = (size_t)(meta[2 * sidx] + r0) * H + (int)((unsigned)u % (unsigned)H);
+            orow0 = (size_t)(meta[2 * sidx] + r0) * H + unit_head(u);
         } else {
-            const Unit un = decode_unit(u, H, NT);
-            orow0 = grow(un, r0, T, H);
+            orow0 = unit_row(u, r0);
         }
         const size_t obase = orow0 * KD + d;
         const uint32_t hk = (uint32_t)H * KD;
@@ -814,8 +826,7 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             const int row = r0 + lane;
             // recomputed here rather than kept live across the unit (register budget)
             const size_t brow =
-                VARLEN ? (size_t)(meta[2 * sidx] + row) * H + (int)((unsigned)u % (unsigned)H)
-                       : grow(decode_unit(u, H, NT), row, T, H);
+                VARLEN ? (size_t)(meta[2 * sidx] + row) * H + unit_head(u) : unit_row(u, row);
             float v = (sdbp[row] + sdbp[BT + row]) + (sdbp[2 * BT + row] + sdbp[3 * BT + row]);
             if (dbg_ok(ex.dbg, brow, ex.nrows, DBG_STORE)) {
                 if constexpr (ACCUM) {

@@ -175,7 +175,7 @@ kda_status_t kda_intra_bwd_host(const void *q, const void *k, const float *g,
  *                  2^(g_r - g_8) * 2^(g_8 - g_s); both exponents are <= 0 (g is
  *                  non-increasing inside a chunk), so nothing can overflow, and the
  *                  quadrant costs four FMAs per (r, s, d) instead of an exp2 and seven
- *                  FP32 operations (about 6% less kernel time).  The result differs
+ *                  FP32 operations (about 4% less kernel time).  The result differs
  *                  from the exact form by rounding only; same accuracy contract.
  *
  * Runs on the tensor-core path (the same accuracy contract as kda_intra_bwd).
