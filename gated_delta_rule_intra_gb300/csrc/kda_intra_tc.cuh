@@ -77,7 +77,9 @@ constexpr int SM_META = SM_TSLOT + 8;        // varlen: per stage {first token r
 constexpr int SM_LUT = SM_META + 16;         // varlen: {first row, valid rows} of this
                                              // CTA's units, two batches of 32
 constexpr int LUT_BATCH = 32;
-constexpr int SM_TOTAL = SM_LUT + 2 * LUT_BATCH * 8;
+constexpr int SM_TRTAB = SM_LUT + 2 * LUT_BATCH * 8;  // per-thread transpose indices
+                                                      // (option instantiations)
+constexpr int SM_TOTAL = SM_TRTAB + 3 * TC_THREADS * 4;
 // extra shared memory of the fold_dg variant: the per-row dg bank [64][128] and the
 // per-(sub-block, channel) totals, double-buffered by unit parity
 constexpr int SM_FOLD_BANK = (SM_TOTAL + 127) / 128 * 128;
@@ -306,6 +308,34 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
 
     int *meta = reinterpret_cast<int *>(smem + SM_META);
     int *lut = reinterpret_cast<int *>(smem + SM_LUT);
+    // The column-side transposes move the same three elements for this thread in every
+    // unit: element x's (source float, destination float, in-chunk row).  The option
+    // instantiations, whose registers are fuller, pack them once into a table read each
+    // unit; the plain ones and those with both incoming gradients and the fold recompute
+    // them (measured faster each way).
+    constexpr bool TRTAB = (ACCUM || FOLD || VARLEN) && !(ACCUM && FOLD);
+    uint32_t *trtab = reinterpret_cast<uint32_t *>(smem + SM_TRTAB);
+    auto tr_index = [&](const int x, int &src, int &dst, int &row) {
+        const int idx = tid + x * TC_THREADS;  // < 1536
+        const int j = idx >= 768 ? 3 : idx >= 256 ? 2 : 1;
+        const int e = idx - 128 * j * (j - 1);
+        // e enumerates the destination floats in order (n/8, k/4, n%8, k%4)
+        const int n = (e >> 7) * 8 + ((e >> 2) & 7);  // s
+        const int kk = ((e >> 5) & 3) * 4 + (e & 3);  // r - 16j
+        src = dablk(j, n >> 4) * 256 + ((n & 15) >> 2) * 64 + (kk >> 3) * 32 + (kk & 7) * 4 +
+              (n & 3);
+        dst = (int)bcol_off(j) / 4 + e;
+        row = BC * j + kk;
+    };
+    if constexpr (TRTAB) {
+#pragma unroll
+        for (int x = 0; x < 3; ++x) {
+            int src, dst, row;
+            tr_index(x, src, dst, row);  // src < 2304, dst < 1536, row < 64
+            trtab[x * TC_THREADS + tid] =
+                ((uint32_t)src << 17) | ((uint32_t)dst << 6) | (uint32_t)row;
+        }
+    }
     // VARLEN: lane j of warp 0 looks up the row range of this CTA's unit k0 + j (two
     // dependent table reads), for the refills of a whole batch of units at once
     auto lookup_batch = [&](const int k0) {
@@ -417,18 +447,18 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             const float *ak = reinterpret_cast<const float *>(st + ST_DK);
 #pragma unroll
             for (int x = 0; x < 3; ++x) {
-                const int idx = tid + x * TC_THREADS;  // < 1536
-                const int j = idx >= 768 ? 3 : idx >= 256 ? 2 : 1;
-                const int e = idx - 128 * j * (j - 1);
-                // e enumerates the destination floats in order (n/8, k/4, n%8, k%4)
-                const int n = (e >> 7) * 8 + ((e >> 2) & 7);  // s
-                const int kk = ((e >> 5) & 3) * 4 + (e & 3);  // r - 16j
-                const int src = dablk(j, n >> 4) * 256 + ((n & 15) >> 2) * 64 + (kk >> 3) * 32 +
-                                (kk & 7) * 4 + (n & 3);
-                trdst[x] = (int)bcol_off(j) / 4 + e;
+                int src, row;
+                if constexpr (TRTAB) {
+                    const uint32_t w = trtab[x * TC_THREADS + tid];
+                    src = (int)(w >> 17);
+                    trdst[x] = (int)((w >> 6) & 2047u);
+                    row = (int)(w & 63u);
+                } else {
+                    tr_index(x, src, trdst[x], row);
+                }
                 trq[x] = aq[src];
                 trk[x] = ak[src];
-                if (VARLEN && BC * j + kk >= ulen) trq[x] = trk[x] = 0.f;
+                if (VARLEN && row >= ulen) trq[x] = trk[x] = 0.f;
             }
         }
 
