@@ -245,3 +245,12 @@ def test_maximum_head_count():
     for name, a, b in zip(("Aqk", "Akk"), fouts, fref):
         a = a[:, :, heads].double().cpu().numpy()
         assert float(np.max(np.abs(a - b)) / np.max(np.abs(b))) <= 2e-3, name
+
+
+@pytest.mark.parametrize("path", _gpu.PATHS)
+def test_many_units_per_cta_with_an_odd_head_count(path):
+    """896 units with H = 7: each persistent CTA runs about six units and the unit's head
+    wraps around H as it advances by the grid stride; every element against the oracle."""
+    cpu = kda_inputs.make_inputs(2, 4096, 7, seed=140)
+    got = _gpu.run(path, _gpu.to_device(cpu))
+    _gpu.assert_close(got, _gpu.oracle_outputs(cpu), _gpu.TOL[path], f"{path} H=7 B=2 T=4096")

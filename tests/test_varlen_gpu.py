@@ -169,3 +169,20 @@ def test_deterministic():
     for x, y in zip(a, b):
         assert torch.equal(x, y)
     assert np.isfinite(a[3].cpu().numpy()).all()
+
+
+def test_more_than_32_units_per_cta():
+    """About 5,000 units with H = 7: every CTA crosses the 32-unit batches of row ranges
+    it looks up ahead, with the head wrapping as it advances; forward and backward."""
+    lens = kda_inputs.varlen_seqlens(45000, seed=141, max_len=3000)
+    cpu, cu = kda_inputs.make_varlen_inputs(lens, 7, seed=142)
+    chunks = int(sum(-(-n // 64) for n in lens))
+    assert chunks * 7 > 32 * 152
+    _gpu.assert_close(run_varlen(cpu, cu), ref_varlen(cpu, cu), TOL, "varlen, many units per CTA")
+    dev = _gpu.to_device(cpu)
+    got = kda.kda_intra_fwd(*(dev[n] for n in ("q", "k", "g", "beta")), cu_seqlens=cu.cuda())
+    ref = oracle.intra_fwd_ex(*(cpu[n] for n in ("q", "k", "g", "beta")), cu_seqlens=cu.numpy())
+    for name, a, b in zip(("Aqk", "Akk"), got, ref):
+        a = a.double().cpu().numpy()
+        err = float(np.max(np.abs(a - b)) / np.max(np.abs(b)))
+        assert err <= TOL, (name, err)
