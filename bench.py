@@ -263,15 +263,15 @@ def config_dict(cfg, path, opts=None):
 
 # --------------------------------------------------------------------------- oracle
 
-def oracle_rate(cpu_inputs, units_sample, bt=64):
+def oracle_rate(cpu_inputs, units_sample, bt=64, nthreads=0):
     """Time the fp64 oracle on a sample; returns (tokens*heads/s, seconds, cores)."""
     import oracle
     lib = oracle.load()
     t = time.perf_counter()
     oracle.intra_bwd(*(cpu_inputs[n] for n in ("q", "k", "g", "beta", "dAqk", "dAkk")),
-                     lib=lib)
+                     lib=lib, nthreads=nthreads)
     dt = time.perf_counter() - t
-    return units_sample * bt / dt, dt, oracle.max_threads(lib)
+    return units_sample * bt / dt, dt, (nthreads or oracle.max_threads(lib))
 
 
 def cpu_baseline(cpu, cfg):
@@ -280,9 +280,16 @@ def cpu_baseline(cpu, cfg):
     sample = {n: v[:nb] for n, v in cpu.items()}
     units = nb * cfg.H * (cfg.T // kda_inputs.BT)
     value, secs, cores = oracle_rate(sample, units)
+    # the same oracle on one thread, on 64 sampled units (scaled by the unit count)
+    few = kda_inputs.sample_units(cfg, 64)
+    one, one_secs, _ = oracle_rate(kda_inputs.gather_units(cpu, few, cfg.H, cfg.T), len(few),
+                                   nthreads=1)
     return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"batch elements 0..{nb - 1} of {cfg.B} ({units} of {cfg.units} "
-                      f"units), one pass, {secs:.2f} s wall on {cores} threads"}
+                      f"units), one pass, {secs:.2f} s wall on {cores} threads",
+            "single_core": {"value": one, "unit": UNIT, "cores": 1,
+                            "sample": f"{len(few)} sampled units, {one_secs:.2f} s, "
+                                      "scaled by unit count"}}
 
 
 def sampled_check(cpu, cfg, outs, n_units=8):
