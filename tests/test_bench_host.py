@@ -1,0 +1,48 @@
+"""The benchmark's byte accounting and its ncu-summary lookup (CPU only)."""
+
+import pytest
+
+import bench
+import kda_inputs
+
+
+def test_algorithmic_bytes_of_the_headline_launch():
+    # q, k 32,768; g 32,768; beta 256; ten lower 16x16 dA blocks x 2 = 20,480;
+    # dq, dk, dg 98,304; db 256
+    assert bench.algorithmic_bytes_per_unit() == 184832
+    assert kda_inputs.CONFIGS[2].units * bench.algorithmic_bytes_per_unit() == 1514143744
+
+
+def test_option_bytes():
+    base = bench.algorithmic_bytes_per_unit()
+    assert bench.algorithmic_bytes_per_unit(accumulate=True) - base == 3 * 64 * 128 * 4 + 64 * 4
+    assert base - bench.algorithmic_bytes_per_unit(io_out=True) == 2 * 64 * 128 * 2
+    assert base - bench.algorithmic_bytes_per_unit(group=4) == 2 * 64 * 128 * 2 * 3 / 4
+    assert bench.FWD_BYTES_PER_UNIT == 98560
+
+
+@pytest.mark.parametrize("lens", [[64], [128, 64], [320]])
+def test_varlen_bytes_of_whole_chunks_equal_the_fixed_length_count(lens):
+    chunks = sum(n // 64 for n in lens)
+    for acc in (False, True):
+        assert bench.varlen_algorithmic_bytes(lens, 3, accumulate=acc) == \
+            3 * chunks * bench.algorithmic_bytes_per_unit(accumulate=acc)
+
+
+def test_varlen_bytes_of_a_short_chunk():
+    # 20 valid rows: per-row tensors for 20 rows, and the lower-block part of their dA
+    # rows (rows 0..15 read one 16-wide block, rows 16..19 two)
+    per_row = (2 * 128 * 2 + 128 * 4 + 4      # q, k (bf16), g, beta
+               + 3 * 128 * 4 + 4)             # dq, dk, dg, db (fp32)
+    da = 2 * 4 * (16 * 16 + 4 * 32)
+    assert bench.varlen_algorithmic_bytes([20], 1) == 20 * per_row + da
+
+
+def test_traffic_is_null_when_the_summary_is_for_other_sources(monkeypatch):
+    name, workload = "kda_intra_bwd_tc_kernel", kda_inputs.CONFIGS[2].name
+    current = bench.ncu_traffic(name, workload)
+    if current is None:
+        pytest.skip("the committed summary predates the current sources")
+    assert current > 0.9 * kda_inputs.CONFIGS[2].units * bench.algorithmic_bytes_per_unit()
+    monkeypatch.setattr(bench, "source_hash", lambda kernel: "0" * 16)
+    assert bench.ncu_traffic(name, workload) is None
