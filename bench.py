@@ -528,7 +528,9 @@ def main():
     p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    p.add_argument("--config", type=int, default=2, help="workload index (2 = headline)")
+    p.add_argument("--config", type=int, default=kda_inputs.HEADLINE,
+                   help="index into kda_inputs.CONFIGS (default: the headline workload, "
+                        "B=8 T=4096 H=16)")
     p.add_argument("--path", choices=tuple(KERNEL_NAMES), default="kda_intra_bwd")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-e2e", action="store_true")

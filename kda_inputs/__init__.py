@@ -60,6 +60,8 @@ CONFIGS = (
     Config("long_B1_T32768_H32", 1, 32768, 32, -1.0),
     Config("gate_stress_B4_T8192_H64_fp16", 4, 8192, 64, -8.0, torch.float16),
 )
+# their positions in CONFIGS (each one's seed is SEED0 + its position)
+SINGLE_CHUNK, SMALL, HEADLINE, LONG, GATE_STRESS = range(len(CONFIGS))
 
 
 def chunk_masks(bt: int = BT):

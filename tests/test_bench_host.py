@@ -10,7 +10,7 @@ def test_algorithmic_bytes_of_the_headline_launch():
     # q, k 32,768; g 32,768; beta 256; ten lower 16x16 dA blocks x 2 = 20,480;
     # dq, dk, dg 98,304; db 256
     assert bench.algorithmic_bytes_per_unit() == 184832
-    assert kda_inputs.CONFIGS[2].units * bench.algorithmic_bytes_per_unit() == 1514143744
+    assert kda_inputs.CONFIGS[kda_inputs.HEADLINE].units * bench.algorithmic_bytes_per_unit() == 1514143744
 
 
 def test_option_bytes():
@@ -39,10 +39,10 @@ def test_varlen_bytes_of_a_short_chunk():
 
 
 def test_traffic_is_null_when_the_summary_is_for_other_sources(monkeypatch):
-    name, workload = "kda_intra_bwd_tc_kernel", kda_inputs.CONFIGS[2].name
+    name, workload = "kda_intra_bwd_tc_kernel", kda_inputs.CONFIGS[kda_inputs.HEADLINE].name
     current = bench.ncu_traffic(name, workload)
     if current is None:
         pytest.skip("the committed summary predates the current sources")
-    assert current > 0.9 * kda_inputs.CONFIGS[2].units * bench.algorithmic_bytes_per_unit()
+    assert current > 0.9 * kda_inputs.CONFIGS[kda_inputs.HEADLINE].units * bench.algorithmic_bytes_per_unit()
     monkeypatch.setattr(bench, "source_hash", lambda kernel: "0" * 16)
     assert bench.ncu_traffic(name, workload) is None

@@ -53,7 +53,7 @@ def test_fast_and_fp32_paths(shape, dtype):
 
 def test_headline_workload():
     """8192 units: every CTA of the persistent grid runs many units and both stages."""
-    dev = _dev(kda_inputs.make_config_inputs(2))
+    dev = _dev(kda_inputs.make_config_inputs(kda_inputs.HEADLINE))
     args = [dev[n] for n in _gpu.ARGS]
     _same_under_checks(lambda: kda.kda_intra_bwd(*args))
     _same_under_checks(lambda: kda.kda_intra_fwd(*args[:4]))

@@ -18,14 +18,14 @@ def run_fd(dev, factor=True, **opts):
     return kda.kda_intra_bwd_ex(*(dev[n] for n in _gpu.ARGS), factor_diag=factor, **opts)
 
 
-@pytest.mark.parametrize("cfg", [0, 1, 2])
+@pytest.mark.parametrize("cfg", [kda_inputs.SINGLE_CHUNK, kda_inputs.SMALL, kda_inputs.HEADLINE])
 def test_configs_every_element(cfg):
     cpu = kda_inputs.make_config_inputs(cfg)
     got = run_fd(_gpu.to_device(cpu))
     _gpu.assert_close(got, _gpu.oracle_outputs(cpu), TOL, f"factor_diag config {cfg}")
 
 
-@pytest.mark.parametrize("cfg", [3, 4])
+@pytest.mark.parametrize("cfg", [kda_inputs.LONG, kda_inputs.GATE_STRESS])
 def test_large_configs_sampled_units(cfg):
     """B=1 T=32768 H=32 and the fp16 gate-stress workload (g down to about -500)."""
     cpu = kda_inputs.make_config_inputs(cfg)
@@ -50,7 +50,7 @@ def test_steep_gates(gate_lo):
 
 def test_close_to_the_exact_diagonal_at_full_size():
     """Same kernel, same inputs: the two diagonal forms differ by rounding only."""
-    cpu = kda_inputs.make_config_inputs(2)
+    cpu = kda_inputs.make_config_inputs(kda_inputs.HEADLINE)
     dev = _gpu.to_device(cpu)
     exact = run_fd(dev, factor=False)
     fact = run_fd(dev, factor=True)

@@ -34,13 +34,13 @@ def assert_fwd_close(got, ref, what):
     assert all(e <= TOL for e in errs.values()), f"{what}: {errs}"
 
 
-@pytest.mark.parametrize("idx", [0, 1, 2])
+@pytest.mark.parametrize("idx", [kda_inputs.SINGLE_CHUNK, kda_inputs.SMALL, kda_inputs.HEADLINE])
 def test_full_workloads(idx):
     cpu = kda_inputs.make_config_inputs(idx)
     assert_fwd_close(run_fwd(cpu), ref_fwd(cpu), kda_inputs.CONFIGS[idx].name)
 
 
-@pytest.mark.parametrize("idx", [3, 4])
+@pytest.mark.parametrize("idx", [kda_inputs.LONG, kda_inputs.GATE_STRESS])
 def test_large_workloads_sampled_units(idx):
     cfg = kda_inputs.CONFIGS[idx]
     cpu = kda_inputs.make_config_inputs(idx)
@@ -99,7 +99,7 @@ def test_forward_and_backward_satisfy_euler_identities():
     """At full size (the headline workload), the two kernels against each other:
     sum q*dq = sum dAqk*Aqk and sum beta*db = sum dAkk*Akk (homogeneity of Aqk in q
     and of Akk in beta)."""
-    cpu = kda_inputs.make_config_inputs(2)
+    cpu = kda_inputs.make_config_inputs(kda_inputs.HEADLINE)
     dev = _gpu.to_device(cpu)
     Aqk, Akk = kda.kda_intra_fwd(*(dev[n] for n in IN))
     dq, dk, db, dg = kda.kda_intra_bwd(*(dev[n] for n in _gpu.ARGS))

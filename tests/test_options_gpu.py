@@ -86,7 +86,7 @@ def test_fold_dg_with_incoming_and_groups():
 def test_fold_dg_is_the_reverse_cumsum_of_the_plain_dg():
     """Property at full size (the headline workload): folding is a chunk-local suffix sum
     of the unfolded dg, checked on the GPU outputs themselves."""
-    cpu = kda_inputs.make_config_inputs(2)
+    cpu = kda_inputs.make_config_inputs(kda_inputs.HEADLINE)
     dev = _gpu.to_device(cpu)
     plain = kda.kda_intra_bwd_ex(*(dev[n] for n in _gpu.ARGS))
     folded = kda.kda_intra_bwd_ex(*(dev[n] for n in _gpu.ARGS), fold_dg=True)
@@ -121,7 +121,7 @@ def test_plain_options_match_the_plain_entry_point():
 
 def test_full_size_all_options():
     """The headline workload with every option on, every element against the oracle."""
-    cpu = kda_inputs.make_config_inputs(2)
+    cpu = kda_inputs.make_config_inputs(kda_inputs.HEADLINE)
     ins = incoming(8, 4096, 16, seed=50)
     got = run_ex(cpu, fold_dg=True, **ins)
     ref = ref_ex(cpu, fold_dg=True, **ins)

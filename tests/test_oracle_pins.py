@@ -44,7 +44,7 @@ def test_finite_differences_full_width_chunk(lib):
 
 
 def _quantised_config0():
-    x = kda_inputs.make_config_inputs(0)
+    x = kda_inputs.make_config_inputs(kda_inputs.SINGLE_CHUNK)
     return {n: v.to(torch.float64).numpy() for n, v in x.items()}
 
 
@@ -61,7 +61,7 @@ def test_config0_against_autograd(lib):
 
 def test_gate_stress_unit_against_autograd(lib):
     """Cumulative gates down to about -300 (fp16 q/k): the separable fp64 form still holds."""
-    cfg = kda_inputs.CONFIGS[4]
+    cfg = kda_inputs.CONFIGS[kda_inputs.GATE_STRESS]
     inp = kda_inputs.make_inputs(1, 128, 2, gate_lo=cfg.gate_lo, qk_dtype=cfg.qk_dtype,
                                  seed=99)
     inp = {n: v.to(torch.float64).numpy() for n, v in inp.items()}

@@ -28,7 +28,7 @@ def config_inputs():
 
 
 @pytest.mark.parametrize("path", _gpu.PATHS)
-@pytest.mark.parametrize("cfg", [0, 1])
+@pytest.mark.parametrize("cfg", [kda_inputs.SINGLE_CHUNK, kda_inputs.SMALL])
 def test_full_parity_small_configs(config_inputs, path, cfg):
     cpu, dev = config_inputs(cfg)
     got = _gpu.run(path, dev)
@@ -38,7 +38,7 @@ def test_full_parity_small_configs(config_inputs, path, cfg):
 
 
 @pytest.mark.parametrize("path", _gpu.PATHS)
-@pytest.mark.parametrize("cfg", [2, 3, 4])
+@pytest.mark.parametrize("cfg", [kda_inputs.HEADLINE, kda_inputs.LONG, kda_inputs.GATE_STRESS])
 def test_full_parity_full_size(config_inputs, path, cfg):
     """Full-size launch (the benchmark's configuration), every element vs the oracle."""
     cpu, dev = config_inputs(cfg)
@@ -198,7 +198,7 @@ def test_misaligned_pointer_is_a_status_not_a_fault():
 
 def test_sampled_units_match_full_launch():
     """The sampled-unit helper the benchmark uses agrees with the full launch."""
-    cpu = kda_inputs.make_config_inputs(1)
+    cpu = kda_inputs.make_config_inputs(kda_inputs.SMALL)
     dev = _gpu.to_device(cpu)
     _gpu.sampled_parity("kda_intra_bwd", 1, cpu, dev, n_units=8)
 
