@@ -217,6 +217,8 @@ def setup_dist():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)  # before the process group: NCCL binds this device
         backend = "nccl" if torch.cuda.is_available() else "gloo"
         dist.init_process_group(backend=backend)
     return world, rank, local
