@@ -58,6 +58,18 @@
 extern "C" {
 #endif
 
+/*
+ * ABI versions (kda_abi_version() returns the loaded library's):
+ *   7  kda_debug_checks, kda_debug_set_flags (the bounds-checked debug build)
+ *   6  kda_intra_bwd_opts_t gains factor_diag (appended; the struct grew)
+ *   5  kda_intra_fwd_ex and kda_intra_fwd_opts_t
+ *   4  kda_intra_fwd
+ *   3  variable-length fields of kda_intra_bwd_opts_t (cu_seqlens .. num_chunks)
+ *   2  kda_intra_bwd_ex and kda_intra_bwd_opts_t
+ *   1  kda_intra_bwd, kda_intra_bwd_fp32, the host entry point, status helpers
+ * Option structs only grow at their end; compile against the header of the library you
+ * load (or check kda_abi_version()) before passing one.
+ */
 #define KDA_ABI_VERSION 7
 #define KDA_BT 64  /* chunk length */
 #define KDA_BC 16  /* sub-block length inside a chunk */
