@@ -14,6 +14,8 @@ The functions carry the C names of ``include/kda.h``:
   factorized (``factor_diag``)
 * ``prepare_chunk_indices`` -- the (sequence, chunk) table of a ``cu_seqlens``
 * ``kda_intra_bwd_host``  -- host buffers in and out, copies on the stream
+* ``kda_intra_bwd_host_static`` -- the same without a workspace, staged in the library's
+  fixed device array (``HOST_STATIC_MAX_BYTES``) for callers that cannot allocate
 * ``kda_intra_fwd``       -- the forward score matrices Aqk, Akk (grouped value heads
   and variable-length sequences through ``kda_intra_fwd_ex``)
 * ``kda_status_str``, ``kda_abi_version``
@@ -38,6 +40,8 @@ KDA_BF16 = 0
 KDA_FP16 = 1
 BT = 64
 K = 128
+KDA_ERR_TOO_LARGE = 10
+HOST_STATIC_MAX_BYTES = 32 << 20  # KDA_HOST_STATIC_MAX_BYTES of include/kda.h
 
 _DTYPES = {torch.bfloat16: KDA_BF16, torch.float16: KDA_FP16}
 _lib = None
@@ -87,6 +91,8 @@ def load_library(path: str | None = None):
     lib.kda_intra_bwd_ex.restype = st
     lib.kda_intra_bwd_host.argtypes = sig[:-1] + [vp, ctypes.c_size_t, vp]
     lib.kda_intra_bwd_host.restype = st
+    lib.kda_intra_bwd_host_static.argtypes = sig
+    lib.kda_intra_bwd_host_static.restype = st
     lib.kda_intra_fwd.argtypes = [vp, vp, fp, fp, fp, fp, i, i, i, i, vp]
     lib.kda_intra_fwd.restype = st
     lib.kda_intra_fwd_ex.argtypes = [vp, vp, fp, fp, fp, fp, i, i, i, i,
@@ -401,4 +407,34 @@ def kda_intra_bwd_host(q, k, g, beta, dAqk, dAkk, dq, dk, db, dg, workspace, str
             _stream_handle(stream, workspace.device))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_intra_bwd_host")
+    return dq, dk, db, dg
+
+
+def kda_intra_bwd_host_static(q, k, g, beta, dAqk, dAkk, dq, dk, db, dg, device=None,
+                              stream=None):
+    """``kda_intra_bwd_host`` without a workspace: for callers holding host tensors
+    that may not allocate device memory.  The device staging is the library's own
+    fixed array of ``HOST_STATIC_MAX_BYTES`` per GPU, so the problem must fit it
+    (``kda_intra_bwd_host_workspace_bytes(B, T, H) <= HOST_STATIC_MAX_BYTES``, else
+    ``KdaError`` with ``KDA_ERR_TOO_LARGE``).  Runs on ``device`` (default: the current
+    CUDA device) and ``stream``; every call shares the one array, so calls must not
+    overlap on the GPU.  Synchronise the stream before reading dq/dk/db/dg.
+    """
+    for n, t in (("q", q), ("k", k), ("g", g), ("beta", beta), ("dAqk", dAqk),
+                 ("dAkk", dAkk), ("dq", dq), ("dk", dk), ("db", db), ("dg", dg)):
+        if t.device.type != "cpu":
+            raise ValueError(f"{n} must be a host tensor")
+    B, T, H = _validate(q, k, g, beta, dAqk, dAkk, dq, dk, db, dg, torch.device("cpu"))
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None \
+        else torch.device(device)
+    lib = load_library()
+    ptr = ctypes.c_void_p
+    with torch.cuda.device(dev):
+        rc = lib.kda_intra_bwd_host_static(
+            ptr(q.data_ptr()), ptr(k.data_ptr()), ptr(g.data_ptr()), ptr(beta.data_ptr()),
+            ptr(dAqk.data_ptr()), ptr(dAkk.data_ptr()), ptr(dq.data_ptr()),
+            ptr(dk.data_ptr()), ptr(db.data_ptr()), ptr(dg.data_ptr()),
+            B, T, H, _DTYPES[q.dtype], _stream_handle(stream, dev))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_intra_bwd_host_static")
     return dq, dk, db, dg

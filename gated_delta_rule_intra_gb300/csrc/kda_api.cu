@@ -2,6 +2,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 #include "kda.h"
@@ -436,6 +438,97 @@ kda_status_t kda_intra_bwd_host(const void *q, const void *k, const float *g,
     return result;
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// kda_intra_bwd_host_static: the host entry point with its device staging in a fixed
+// array of this library, for callers that may not allocate device memory.
+
+// The staging buffers.  Every GPU on which this module is loaded holds it until the
+// process exits.  Host code must not pass this name to a kernel: on the host it is a
+// stand-in, not a device address; scratch_base() looks the address up.
+static __device__ __align__(256) unsigned char g_host_scratch[KDA_HOST_STATIC_MAX_BYTES];
+
+namespace {
+
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices];  // device address of g_host_scratch, per device
+
+// The array's device address on the current device, looked up on the first call there.
+kda_status_t scratch_base(char **base) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return KDA_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_host_scratch) != cudaSuccess || !p)
+            return KDA_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *base = (char *)g_scratch_addr[dev];
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status_t kda_intra_bwd_host_static(const void *q, const void *k, const float *g,
+                                       const float *beta, const float *dAqk,
+                                       const float *dAkk, float *dq, float *dk, float *db,
+                                       float *dg, int B, int T, int H, kda_dtype_t qk_dtype,
+                                       kda_stream_t stream) {
+    kda_status_t st = check_args(q, k, g, beta, dAqk, dAkk, dq, dk, db, dg, B, T, H,
+                                 qk_dtype, false);
+    if (st != KDA_OK) return st;
+    if (kda_intra_bwd_host_workspace_bytes(B, T, H, qk_dtype) > KDA_HOST_STATIC_MAX_BYTES)
+        return KDA_ERR_TOO_LARGE;
+    if ((st = check_device()) != KDA_OK) return st;
+    char *w = nullptr;
+    if ((st = scratch_base(&w)) != KDA_OK) return st;
+    (void)cudaGetLastError();
+
+    // Same carving as kda_intra_bwd_host.  The uploads overwrite every input byte and
+    // the kernel every output byte, so the previous call's contents never leak in.
+    const size_t rows = (size_t)B * T * H;
+    const size_t nqk = rows * KDA_K * 2, nk4 = rows * KDA_K * 4, nrow = rows * 4,
+                 nda = rows * KDA_BT * 4;
+    char *dq_d = w;                 w += align256(nk4);
+    char *dk_d = w;                 w += align256(nk4);
+    char *dg_d = w;                 w += align256(nk4);
+    char *db_d = w;                 w += align256(nrow);
+    char *q_d = w;                  w += align256(nqk);
+    char *k_d = w;                  w += align256(nqk);
+    char *g_d = w;                  w += align256(nk4);
+    char *beta_d = w;               w += align256(nrow);
+    char *aqk_d = w;                w += align256(nda);
+    char *akk_d = w;
+
+    // One stream, in order: uploads, the kernel, downloads.  At these sizes there is
+    // nothing to gain from the pipelined pieces of kda_intra_bwd_host.
+    const cudaStream_t s = (cudaStream_t)stream;
+    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+    if (cudaMemcpyAsync(q_d, q, nqk, h2d, s) != cudaSuccess ||
+        cudaMemcpyAsync(k_d, k, nqk, h2d, s) != cudaSuccess ||
+        cudaMemcpyAsync(g_d, g, nk4, h2d, s) != cudaSuccess ||
+        cudaMemcpyAsync(beta_d, beta, nrow, h2d, s) != cudaSuccess ||
+        cudaMemcpyAsync(aqk_d, dAqk, nda, h2d, s) != cudaSuccess ||
+        cudaMemcpyAsync(akk_d, dAkk, nda, h2d, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    st = kda_intra_bwd(q_d, k_d, (const float *)g_d, (const float *)beta_d,
+                       (const float *)aqk_d, (const float *)akk_d, (float *)dq_d,
+                       (float *)dk_d, (float *)db_d, (float *)dg_d, B, T, H, qk_dtype,
+                       stream);
+    if (st != KDA_OK) return st;
+    if (cudaMemcpyAsync(dq, dq_d, nk4, d2h, s) != cudaSuccess ||
+        cudaMemcpyAsync(dk, dk_d, nk4, d2h, s) != cudaSuccess ||
+        cudaMemcpyAsync(dg, dg_d, nk4, d2h, s) != cudaSuccess ||
+        cudaMemcpyAsync(db, db_d, nrow, d2h, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
 const char *kda_status_str(kda_status_t status) {
     switch (status) {
         case KDA_OK: return "KDA_OK";
@@ -451,6 +544,10 @@ const char *kda_status_str(kda_status_t status) {
         case KDA_ERR_OVERLAP: return "KDA_ERR_OVERLAP: argument buffers overlap";
         case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing or too small";
         case KDA_ERR_OPTION: return "KDA_ERR_OPTION: unsupported option combination";
+        case KDA_ERR_TOO_LARGE:
+            return "KDA_ERR_TOO_LARGE: the problem needs more than the library's fixed "
+                   "32 MiB of staging (KDA_HOST_STATIC_MAX_BYTES); use kda_intra_bwd_host "
+                   "with a workspace";
     }
     return "KDA_ERR_UNKNOWN";
 }

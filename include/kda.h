@@ -60,6 +60,7 @@ extern "C" {
 
 /*
  * ABI versions (kda_abi_version() returns the loaded library's):
+ *   8  kda_intra_bwd_host_static, KDA_HOST_STATIC_MAX_BYTES, KDA_ERR_TOO_LARGE
  *   7  kda_debug_checks, kda_debug_set_flags (the bounds-checked debug build)
  *   6  kda_intra_bwd_opts_t gains factor_diag (appended; the struct grew)
  *   5  kda_intra_fwd_ex and kda_intra_fwd_opts_t
@@ -70,7 +71,7 @@ extern "C" {
  * Option structs only grow at their end; compile against the header of the library you
  * load (or check kda_abi_version()) before passing one.
  */
-#define KDA_ABI_VERSION 7
+#define KDA_ABI_VERSION 8
 #define KDA_BT 64  /* chunk length */
 #define KDA_BC 16  /* sub-block length inside a chunk */
 #define KDA_K 128  /* head dimension */
@@ -90,8 +91,11 @@ typedef enum {
     KDA_ERR_UNSUPPORTED_DEVICE = 6, /* current device is not compute capability 10.3 */
     KDA_ERR_OVERLAP = 7,            /* two argument buffers overlap */
     KDA_ERR_WORKSPACE = 8,          /* workspace missing or too small (*_host only) */
-    KDA_ERR_OPTION = 9              /* unsupported option combination (*_ex), or debug
+    KDA_ERR_OPTION = 9,             /* unsupported option combination (*_ex), or debug
                                        reporting asked of a build without checks */
+    KDA_ERR_TOO_LARGE = 10          /* the call needs more scratch than the library's
+                                       fixed KDA_HOST_STATIC_MAX_BYTES
+                                       (kda_intra_bwd_host_static only) */
 } kda_status_t;
 
 typedef enum { KDA_BF16 = 0, KDA_FP16 = 1 } kda_dtype_t;
@@ -142,6 +146,42 @@ kda_status_t kda_intra_bwd_host(const void *q, const void *k, const float *g,
                                 int B, int T, int H, kda_dtype_t qk_dtype,
                                 void *workspace, size_t workspace_bytes,
                                 kda_stream_t stream);
+
+/*
+ * kda_intra_bwd_host without a workspace argument, for callers that hold only host
+ * buffers and may not allocate device memory: a plugin or FFI caller inside a host
+ * application whose device memory is owned by another allocator (a framework's
+ * caching pool that has reserved it, a fixed per-process budget), or code on a
+ * latency-critical path where cudaMalloc's implicit device synchronisation is not
+ * acceptable.  The paper has no counterpart for this entry point; it is a deployment
+ * convenience around the same kernel.
+ *
+ * The device staging buffers live in one array of this library, KDA_HOST_STATIC_MAX_BYTES
+ * (32 MiB) of global memory that every GPU on which the library's device code is loaded
+ * holds until the process exits.  A call whose staging need,
+ * kda_intra_bwd_host_workspace_bytes(B, T, H, qk_dtype), exceeds it returns
+ * KDA_ERR_TOO_LARGE before anything is queued.  The need is 3080 bytes per token-head
+ * row, so up to B*T*H = 10,880 rows fit (for instance B = 2, T = 1024, H = 4); larger
+ * problems take kda_intra_bwd_host with a caller-owned workspace.  The call allocates
+ * nothing (no cudaMalloc, no cudaFree, no stream, no event): it queues the six uploads,
+ * the kernel and the four downloads, in that order, on `stream` and returns.
+ * Synchronise `stream` before reading the outputs or reusing the inputs.
+ *
+ * The first call on each device looks up the array's device address (with that device
+ * current); make that first call before any stream capture on that device.  Every call,
+ * on every stream and thread, shares the one array: calls whose work overlaps on the GPU
+ * race on it, so order them on one stream (or synchronise between them).  The array keeps
+ * the last call's contents; nothing in it needs to start at zero, since each call
+ * overwrites every byte it reads.  Same arguments, status codes and accuracy as
+ * kda_intra_bwd_host otherwise.
+ */
+#define KDA_HOST_STATIC_MAX_BYTES 33554432u /* 32 MiB */
+
+kda_status_t kda_intra_bwd_host_static(const void *q, const void *k, const float *g,
+                                       const float *beta, const float *dAqk,
+                                       const float *dAkk, float *dq, float *dk,
+                                       float *db, float *dg, int B, int T, int H,
+                                       kda_dtype_t qk_dtype, kda_stream_t stream);
 
 /*
  * Options of kda_intra_bwd_ex.  Zero-initialise, then set what you need; a zeroed
