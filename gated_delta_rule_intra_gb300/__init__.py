@@ -35,6 +35,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkda.so")
 DEBUG_LIB_PATH = os.path.join(_HERE, "libkda_debug.so")
 
+# KDA_ABI_VERSION of the include/kda.h these ctypes mirrors follow (option structs,
+# signatures); a library of any other version is refused at load.
+ABI_VERSION = 8
 KDA_OK = 0
 KDA_BF16 = 0
 KDA_FP16 = 1
@@ -108,6 +111,10 @@ def load_library(path: str | None = None):
     lib.kda_debug_checks.restype = i
     lib.kda_debug_set_flags.argtypes = [vp]
     lib.kda_debug_set_flags.restype = st
+    if lib.kda_abi_version() != ABI_VERSION:
+        raise RuntimeError(
+            f"{p} has ABI version {lib.kda_abi_version()}, this binding needs {ABI_VERSION}: "
+            "rebuild it with gated_delta_rule_intra_gb300.build.build_library()")
     if path is None:
         _lib = lib
     return lib
@@ -356,6 +363,7 @@ def kda_intra_fwd(q, k, g, beta, Aqk=None, Akk=None, *, cu_seqlens=None, chunk_i
     dev, f32 = q.device, torch.float32
     Aqk = torch.empty(B, T, HV, BT, device=dev, dtype=f32) if Aqk is None else Aqk
     Akk = torch.empty(B, T, HV, BT, device=dev, dtype=f32) if Akk is None else Akk
+    _check("q", q, (B, T, H, K), q.dtype, dev)
     _check("k", k, (B, T, H, K), q.dtype, dev)
     _check("g", g, (B, T, HV, K), f32, dev)
     _check("beta", beta, (B, T, HV), f32, dev)
