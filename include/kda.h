@@ -48,6 +48,15 @@
  * synchronisation and no device allocation happens inside.  Inputs are not modified.
  * Argument errors are reported before anything is launched; no call aborts the
  * process.
+ *
+ * Stalled pipelines: every wait of a kernel on its own copies or tensor-core work is
+ * bounded (about 4M polls).  A wait that gives up does not hang or trap: the kernel
+ * writes NaN into the outputs of the unit it was working on and carries on.  The call
+ * has already returned KDA_OK when this happens (the status only covers the arguments
+ * and the launch), so in the normal build a stalled pipeline is seen only as NaN
+ * outputs, which NaN or Inf inputs can also produce.  The bounds-checked debug build
+ * (kda_debug_set_flags below) also sets KDA_DBG_WAIT in its flag word, which tells the
+ * two apart.  No valid input makes a wait give up on a healthy GPU.
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -68,8 +77,11 @@ extern "C" {
  *   3  variable-length fields of kda_intra_bwd_opts_t (cu_seqlens .. num_chunks)
  *   2  kda_intra_bwd_ex and kda_intra_bwd_opts_t
  *   1  kda_intra_bwd, kda_intra_bwd_fp32, the host entry point, status helpers
- * Option structs only grow at their end; compile against the header of the library you
- * load (or check kda_abi_version()) before passing one.
+ * Option structs only grow at their end, and the library reads sizeof(its own struct)
+ * from the pointer it is given.  A caller compiled against an older header would have
+ * the library read past the end of its struct, so a caller that passes an option struct
+ * must check at start-up that kda_abi_version() equals the KDA_ABI_VERSION it was
+ * compiled with (the Python binding refuses to load any other version).
  */
 #define KDA_ABI_VERSION 8
 #define KDA_BT 64  /* chunk length */
@@ -133,8 +145,11 @@ kda_status_t kda_intra_bwd_fp32(const void *q, const void *k, const float *g,
  * and db comes down whole after the last): uploads run on one internal stream,
  * downloads on another and the kernels on `stream`, so both copy directions and the
  * compute overlap; events order it all after earlier work on `stream`, and `stream`
- * waits for the last download.  Copies are truly asynchronous only when the host
- * buffers are page-locked.  The call returns once everything is queued: synchronise
+ * waits for the last copy of each direction (also when a call fails midway).  The two
+ * internal streams and their events are made by the first call on each device and
+ * kept until the process exits; calls from several threads queue their work one call
+ * after another on them.  Copies are truly asynchronous only when the host buffers
+ * are page-locked.  The call returns once everything is queued: synchronise
  * `stream` before reading the outputs or reusing the inputs.  Host pointers need no
  * particular alignment.
  */

@@ -44,6 +44,7 @@ def test_abi_version(lib):
     text = open(HEADER).read()
     want = int(re.search(r"#define KDA_ABI_VERSION (\d+)", text).group(1))
     assert kda.kda_abi_version() == want
+    assert kda.ABI_VERSION == want  # the binding's struct mirrors follow this header
 
 
 def test_status_strings(lib):
