@@ -175,6 +175,41 @@ kda::BwdArgs pack(const void *q, const void *k, const float *g, const float *bet
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// kda_intra_bwd_host's internal streams and events, made once per device.
+constexpr int kMaxPieces = 64;
+struct HostPipe {
+    std::mutex mu;  // held while one call enqueues its work
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev[2 * kMaxPieces + 5] = {};
+};
+std::mutex g_pipe_mu;
+HostPipe *g_pipe[kMaxDevices];
+
+kda_status_t host_pipe(HostPipe **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return KDA_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    if (!g_pipe[dev]) {
+        HostPipe *hp = new HostPipe;
+        bool ok = cudaStreamCreateWithFlags(&hp->s_in, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&hp->s_out, cudaStreamNonBlocking) == cudaSuccess;
+        for (cudaEvent_t &e : hp->ev)
+            ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) {
+            for (cudaEvent_t e : hp->ev)
+                if (e) cudaEventDestroy(e);
+            if (hp->s_in) cudaStreamDestroy(hp->s_in);
+            if (hp->s_out) cudaStreamDestroy(hp->s_out);
+            delete hp;
+            return KDA_ERR_CUDA;
+        }
+        g_pipe[dev] = hp;
+    }
+    *out = g_pipe[dev];
+    return KDA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -346,95 +381,97 @@ kda_status_t kda_intra_bwd_host(const void *q, const void *k, const float *g,
     // of piece p+1 go up on one internal stream while piece p computes on the caller's
     // stream and piece p-1 comes down on another, so both copy directions and the
     // kernel overlap.  Events order everything after earlier work on the caller's
-    // stream, and the caller's stream waits for the last copy.  Every copy carries a
-    // fixed cost of a few microseconds, so pieces are large (about 96 MB of input:
-    // fewer copies, against a longer pipeline fill and drain), and beta and db, 1/128
-    // of the rows' bytes, move whole: beta before the first piece, db after the last.
-    // A second copy stream per direction measured slower (the copies contend).
+    // stream, and the caller's stream waits for the last copy of each direction.  Every
+    // copy carries a fixed cost of a few microseconds, so pieces are large (about 96 MB
+    // of input: fewer copies, against a longer pipeline fill and drain), and beta and
+    // db, 1/128 of the rows' bytes, move whole: beta before the first piece, db after
+    // the last.  A second copy stream per direction measured slower (the copies contend).
     const long long chunks = (long long)B * T / KDA_BT;
     const size_t in_bytes = 2 * nqk + nk4 + nrow + 2 * nda;
     long long P = (long long)(in_bytes / ((size_t)96 << 20));
     if (P < 1) P = 1;
-    if (P > 64) P = 64;
+    if (P > kMaxPieces) P = kMaxPieces;
     if (P > chunks) P = chunks;
-    cudaStream_t s = (cudaStream_t)stream, s_in = nullptr, s_out = nullptr;
-    cudaEvent_t ev[2 * 64 + 4] = {};
-    const int nev = (int)(2 * P + 4);
+
+    // The internal streams and events of this device, made on its first call and kept.
+    // The lock makes each call's enqueue sequence contiguous, so an event is recorded
+    // again only after every wait on its previous record has been issued (a wait binds
+    // to the record current when it is issued).  Calls from several threads therefore
+    // queue their copies one call after another on the shared internal streams.
+    HostPipe *hp = nullptr;
+    if ((st = host_pipe(&hp)) != KDA_OK) return st;
+    std::lock_guard<std::mutex> lock(hp->mu);
+    cudaStream_t s = (cudaStream_t)stream, s_in = hp->s_in, s_out = hp->s_out;
+    cudaEvent_t *ev = hp->ev;
     kda_status_t result = KDA_OK;
     auto fail = [&](kda_status_t code) {
         if (result == KDA_OK) result = code;
     };
-    if (cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking) != cudaSuccess)
-        fail(KDA_ERR_CUDA);
-    for (int e = 0; e < nev && result == KDA_OK; ++e)
-        if (cudaEventCreateWithFlags(&ev[e], cudaEventDisableTiming) != cudaSuccess)
-            fail(KDA_ERR_CUDA);
     const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
-    if (result == KDA_OK) {
-        cudaEvent_t e_start = ev[0], e_done = ev[1], e_beta = ev[2 * P + 2],
-                    e_last = ev[2 * P + 3];
-        if (cudaEventRecord(e_start, s) != cudaSuccess ||
-            cudaStreamWaitEvent(s_in, e_start, 0) != cudaSuccess ||
-            cudaStreamWaitEvent(s_out, e_start, 0) != cudaSuccess ||
-            cudaMemcpyAsync(beta_d, beta, nrow, h2d, s_in) != cudaSuccess ||
-            cudaEventRecord(e_beta, s_in) != cudaSuccess ||
-            cudaStreamWaitEvent(s, e_beta, 0) != cudaSuccess)
-            fail(KDA_ERR_CUDA);
-        for (long long p = 0; p < P && result == KDA_OK; ++p) {
-            const long long c0 = p * chunks / P, c1 = (p + 1) * chunks / P;
-            const size_t r0 = (size_t)c0 * KDA_BT * H, nr = (size_t)(c1 - c0) * KDA_BT * H;
-            const int Tp = (int)((c1 - c0) * KDA_BT);
-            cudaEvent_t e_in = ev[2 + 2 * p], e_k = ev[3 + 2 * p];
-            const size_t oqk = r0 * KDA_K * 2, o4 = r0 * KDA_K * 4, orow = r0 * 4,
-                         oda = r0 * KDA_BT * 4;
-            const size_t lqk = nr * KDA_K * 2, l4 = nr * KDA_K * 4, lda = nr * KDA_BT * 4;
-            if (cudaMemcpyAsync(q_d + oqk, (const char *)q + oqk, lqk, h2d, s_in) != cudaSuccess ||
-                cudaMemcpyAsync(k_d + oqk, (const char *)k + oqk, lqk, h2d, s_in) != cudaSuccess ||
-                cudaMemcpyAsync(g_d + o4, (const char *)g + o4, l4, h2d, s_in) != cudaSuccess ||
-                cudaMemcpyAsync(aqk_d + oda, (const char *)dAqk + oda, lda, h2d, s_in) !=
-                    cudaSuccess ||
-                cudaMemcpyAsync(akk_d + oda, (const char *)dAkk + oda, lda, h2d, s_in) !=
-                    cudaSuccess ||
-                cudaEventRecord(e_in, s_in) != cudaSuccess ||
-                cudaStreamWaitEvent(s, e_in, 0) != cudaSuccess) {
-                fail(KDA_ERR_CUDA);
-                break;
-            }
-            const kda_status_t st2 = kda_intra_bwd(
-                q_d + oqk, k_d + oqk, (const float *)(g_d + o4), (const float *)(beta_d + orow),
-                (const float *)(aqk_d + oda), (const float *)(akk_d + oda),
-                (float *)(dq_d + o4), (float *)(dk_d + o4), (float *)(db_d + orow),
-                (float *)(dg_d + o4), 1, Tp, H, qk_dtype, stream);
-            if (st2 != KDA_OK) {
-                fail(st2);
-                break;
-            }
-            if (cudaEventRecord(e_k, s) != cudaSuccess ||
-                cudaStreamWaitEvent(s_out, e_k, 0) != cudaSuccess ||
-                cudaMemcpyAsync((char *)dq + o4, dq_d + o4, l4, d2h, s_out) != cudaSuccess ||
-                cudaMemcpyAsync((char *)dk + o4, dk_d + o4, l4, d2h, s_out) != cudaSuccess ||
-                cudaMemcpyAsync((char *)dg + o4, dg_d + o4, l4, d2h, s_out) != cudaSuccess) {
-                fail(KDA_ERR_CUDA);
-                break;
-            }
-        }
-        // db of every piece, once the last kernel is done
-        if (result == KDA_OK &&
-            (cudaEventRecord(e_last, s) != cudaSuccess ||
-             cudaStreamWaitEvent(s_out, e_last, 0) != cudaSuccess ||
-             cudaMemcpyAsync(db, db_d, nrow, d2h, s_out) != cudaSuccess))
-            fail(KDA_ERR_CUDA);
-        // the caller's stream waits for the last copy, also after a failure midway
-        if (cudaEventRecord(e_done, s_out) != cudaSuccess ||
-            cudaStreamWaitEvent(s, e_done, 0) != cudaSuccess)
-            fail(KDA_ERR_CUDA);
+    cudaEvent_t e_start = ev[0], e_done = ev[1], e_beta = ev[2 * P + 2],
+                e_last = ev[2 * P + 3], e_in_done = ev[2 * P + 4];
+    if (cudaEventRecord(e_start, s) != cudaSuccess ||
+        cudaStreamWaitEvent(s_in, e_start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(s_out, e_start, 0) != cudaSuccess) {
+        fail(KDA_ERR_CUDA);
+        return result;  // nothing is queued on the internal streams
     }
-    // released once their queued work is done; nothing here waits for it
-    for (int e = 0; e < nev; ++e)
-        if (ev[e]) cudaEventDestroy(ev[e]);
-    if (s_in) cudaStreamDestroy(s_in);
-    if (s_out) cudaStreamDestroy(s_out);
+    if (cudaMemcpyAsync(beta_d, beta, nrow, h2d, s_in) != cudaSuccess ||
+        cudaEventRecord(e_beta, s_in) != cudaSuccess ||
+        cudaStreamWaitEvent(s, e_beta, 0) != cudaSuccess)
+        fail(KDA_ERR_CUDA);
+    for (long long p = 0; p < P && result == KDA_OK; ++p) {
+        const long long c0 = p * chunks / P, c1 = (p + 1) * chunks / P;
+        const size_t r0 = (size_t)c0 * KDA_BT * H, nr = (size_t)(c1 - c0) * KDA_BT * H;
+        const int Tp = (int)((c1 - c0) * KDA_BT);
+        cudaEvent_t e_in = ev[2 + 2 * p], e_k = ev[3 + 2 * p];
+        const size_t oqk = r0 * KDA_K * 2, o4 = r0 * KDA_K * 4, orow = r0 * 4,
+                     oda = r0 * KDA_BT * 4;
+        const size_t lqk = nr * KDA_K * 2, l4 = nr * KDA_K * 4, lda = nr * KDA_BT * 4;
+        if (cudaMemcpyAsync(q_d + oqk, (const char *)q + oqk, lqk, h2d, s_in) != cudaSuccess ||
+            cudaMemcpyAsync(k_d + oqk, (const char *)k + oqk, lqk, h2d, s_in) != cudaSuccess ||
+            cudaMemcpyAsync(g_d + o4, (const char *)g + o4, l4, h2d, s_in) != cudaSuccess ||
+            cudaMemcpyAsync(aqk_d + oda, (const char *)dAqk + oda, lda, h2d, s_in) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(akk_d + oda, (const char *)dAkk + oda, lda, h2d, s_in) !=
+                cudaSuccess ||
+            cudaEventRecord(e_in, s_in) != cudaSuccess ||
+            cudaStreamWaitEvent(s, e_in, 0) != cudaSuccess) {
+            fail(KDA_ERR_CUDA);
+            break;
+        }
+        const kda_status_t st2 = kda_intra_bwd(
+            q_d + oqk, k_d + oqk, (const float *)(g_d + o4), (const float *)(beta_d + orow),
+            (const float *)(aqk_d + oda), (const float *)(akk_d + oda),
+            (float *)(dq_d + o4), (float *)(dk_d + o4), (float *)(db_d + orow),
+            (float *)(dg_d + o4), 1, Tp, H, qk_dtype, stream);
+        if (st2 != KDA_OK) {
+            fail(st2);
+            break;
+        }
+        if (cudaEventRecord(e_k, s) != cudaSuccess ||
+            cudaStreamWaitEvent(s_out, e_k, 0) != cudaSuccess ||
+            cudaMemcpyAsync((char *)dq + o4, dq_d + o4, l4, d2h, s_out) != cudaSuccess ||
+            cudaMemcpyAsync((char *)dk + o4, dk_d + o4, l4, d2h, s_out) != cudaSuccess ||
+            cudaMemcpyAsync((char *)dg + o4, dg_d + o4, l4, d2h, s_out) != cudaSuccess) {
+            fail(KDA_ERR_CUDA);
+            break;
+        }
+    }
+    // db of every piece, once the last kernel is done
+    if (result == KDA_OK &&
+        (cudaEventRecord(e_last, s) != cudaSuccess ||
+         cudaStreamWaitEvent(s_out, e_last, 0) != cudaSuccess ||
+         cudaMemcpyAsync(db, db_d, nrow, d2h, s_out) != cudaSuccess))
+        fail(KDA_ERR_CUDA);
+    // The caller's stream waits for the last copy of both directions, also after a
+    // failure midway: no upload still reading the caller's host inputs, and no
+    // download still writing its outputs, outlives the caller's stream.
+    if (cudaEventRecord(e_done, s_out) != cudaSuccess ||
+        cudaEventRecord(e_in_done, s_in) != cudaSuccess ||
+        cudaStreamWaitEvent(s, e_done, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(s, e_in_done, 0) != cudaSuccess)
+        fail(KDA_ERR_CUDA);
     return result;
 }
 
