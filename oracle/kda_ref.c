@@ -47,14 +47,6 @@ static int check_args(int B, int T, int H, int K, int BT) {
     return 0;
 }
 
-static void set_threads(int nthreads) {
-#ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
-#else
-    (void)nthreads;
-#endif
-}
-
 int kda_oracle_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();
@@ -63,15 +55,21 @@ int kda_oracle_max_threads(void) {
 #endif
 }
 
+/* Threads for one call: nthreads if positive, else every available one.  Given to each
+   parallel region on its own, so one call's count never carries over to the next. */
+static int call_threads(int nthreads) {
+    return nthreads > 0 ? nthreads : kda_oracle_max_threads();
+}
+
 /* Forward: the two intra-chunk score matrices. */
 int kda_intra_fwd_ref_f64(const double *q, const double *k, const double *g,
                           const double *beta, double *Aqk, double *Akk,
                           int B, int T, int H, int K, int BT, int nthreads) {
     if (check_args(B, T, H, K, BT)) return -1;
-    set_threads(nthreads);
+    const int nt = call_threads(nthreads);
     const int NT = T / BT;
     const long units = (long)B * H * NT;
-#pragma omp parallel for schedule(dynamic, 1)
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
     for (long u = 0; u < units; ++u) {
         const int h = (int)(u % H);
         const int c = (int)((u / H) % NT);
@@ -102,10 +100,10 @@ int kda_intra_bwd_ref_f64(const double *q, const double *k, const double *g,
                           double *dq, double *dk, double *db, double *dg,
                           int B, int T, int H, int K, int BT, int nthreads) {
     if (check_args(B, T, H, K, BT)) return -1;
-    set_threads(nthreads);
+    const int nt = call_threads(nthreads);
     const int NT = T / BT;
     const long units = (long)B * H * NT;
-#pragma omp parallel for schedule(dynamic, 1)
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
     for (long u = 0; u < units; ++u) {
         const int h = (int)(u % H);
         const int c = (int)((u / H) % NT);
