@@ -7,6 +7,10 @@ One step = one call of the library's intra-chunk backward over the whole workloa
 (the B=8, T=4096, H=16 headline case by default: 8192 units of one (batch, head,
 64-token chunk)), inputs resident in HBM.  The working set (1.61 GB read+written)
 is far larger than the 129 MB L2, so steps run back to back without an L2 flush.
+``--config`` picks another workload (an index, a name such as ``gate_stress``, or
+``all`` for one JSON line per workload).  A workload whose bytes fit in twice the L2
+(the single chunk and the small case) is timed call by call with a 258 MB write
+between calls that evicts the L2, and its line adds the host cost per call.
 
 Under torchrun (N > 1) every rank runs its own independent shard of the same size
 (weak scaling, no collective on the data path); rank 0 prints the JSON line.
@@ -37,7 +41,7 @@ import kda_inputs  # noqa: E402
 
 METRIC = "KDA intra-chunk bwd tokens·heads/s and achieved HBM GB/s (B=8,T=4096,H=16)"
 UNIT = "tokens*heads/s"
-FALLBACK_HBM_GBS = 6800.0
+FALLBACK_HBM_GBS = 8000.0  # nominal GB300 HBM3e, used only without MEASURED_PEAKS.json
 L2_BYTES = 129 * 2 ** 20
 KERNEL_NAMES = {
     "kda_intra_bwd": "kda_intra_bwd_tc_kernel",
@@ -239,7 +243,7 @@ def max_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
-def config_dict(cfg, path, opts=None):
+def config_dict(cfg, path, opts=None, flushed=False):
     d = {
         "workload": cfg.name, "B": cfg.B, "T": cfg.T, "H": cfg.H, "K": kda_inputs.K,
         "BT": kda_inputs.BT, "BC": 16, "units": cfg.units,
@@ -253,6 +257,9 @@ def config_dict(cfg, path, opts=None):
             cfg.units * FWD_BYTES_PER_UNIT / 1e9)
     if opts:
         d["options"] = opts
+    if flushed:
+        d["l2"] = ("flushed: a 258 MB write before every call; each call timed alone "
+                   "with CUDA events (the workload fits in the 129 MB L2)")
     if isinstance(cfg, VarlenWorkload):
         d["sequences"] = {"count": len(cfg.lens), "min": min(cfg.lens), "max": max(cfg.lens),
                           "not_whole_chunks": sum(1 for n in cfg.lens if n % kda_inputs.BT),
@@ -261,6 +268,31 @@ def config_dict(cfg, path, opts=None):
         d["l2"] = "no flush: inputs+outputs of one step (%.2f GB) exceed the 129 MB L2" % (
             varlen_algorithmic_bytes(cfg.lens, cfg.H) / 1e9)
     return d
+
+
+CONFIG_ALIASES = {"single_chunk": kda_inputs.SINGLE_CHUNK, "small": kda_inputs.SMALL,
+                  "headline": kda_inputs.HEADLINE, "long": kda_inputs.LONG,
+                  "gate_stress": kda_inputs.GATE_STRESS}
+
+
+def parse_configs(text: str):
+    """--config value -> list of indices into kda_inputs.CONFIGS: an index, a short
+    name (single_chunk, small, headline, long, gate_stress), a workload name, or
+    'all'."""
+    t = str(text).strip().lower()
+    if t == "all":
+        return list(range(len(kda_inputs.CONFIGS)))
+    if t.lstrip("-").isdigit():
+        i = int(t)
+        if not 0 <= i < len(kda_inputs.CONFIGS):
+            raise ValueError(f"--config {i}: no such workload")
+        return [i]
+    if t in CONFIG_ALIASES:
+        return [CONFIG_ALIASES[t]]
+    for i, c in enumerate(kda_inputs.CONFIGS):
+        if c.name.lower() == t:
+            return [i]
+    raise ValueError(f"--config {text!r}: unknown workload")
 
 
 # --------------------------------------------------------------------------- oracle
@@ -356,6 +388,115 @@ def run_reference(args, cfg):
 
 # --------------------------------------------------------------------------- ours
 
+def launch_bytes(args, cfg, qk_bytes: int, fwd: bool) -> float:
+    """Algorithmic bytes of one launch of the path and options being timed."""
+    if fwd:
+        # per valid token row and head: q, k, g, beta in; both 64-column rows out
+        per_row = 2 * kda_inputs.K * qk_bytes / args.gva + kda_inputs.K * 4 + 4 + 2 * 64 * 4
+        rows = cfg.T * cfg.B if args.varlen else cfg.units * kda_inputs.BT / cfg.H
+        return rows * cfg.H * per_row
+    if args.varlen:
+        b = varlen_algorithmic_bytes(cfg.lens, cfg.H, qk_bytes, accumulate=args.accumulate,
+                                     io_out=args.io_dtype_out)
+        if args.gva > 1:
+            b -= cfg.T * cfg.H * 2 * kda_inputs.K * qk_bytes * (1 - 1 / args.gva)
+        return b
+    return cfg.units * algorithmic_bytes_per_unit(
+        qk_bytes, group=args.gva, accumulate=args.accumulate, io_out=args.io_dtype_out)
+
+
+def host_cost(step, c_call, dev, n=200):
+    """Host wall time per call of n back-to-back calls with no synchronisation between
+    them (fewer than the launch queue holds, so the host never waits for the GPU):
+    through the C ABI directly (ctypes, arguments built once) and through the Python
+    binding (argument checks and marshalling included)."""
+    def per_call(f):
+        torch.cuda.synchronize(dev)
+        t = time.perf_counter()
+        for _ in range(n):
+            f()
+        secs = time.perf_counter() - t
+        torch.cuda.synchronize(dev)
+        return 1e6 * secs / n
+    res = {"calls": n}
+    if c_call is not None:
+        per_call(c_call)
+        res["c_abi_us_per_call"] = per_call(c_call)
+    res["binding_us_per_call"] = per_call(step)
+    return res
+
+
+def end_to_end(kda, args, cfg, cpu, outs, stream, dev, world):
+    """The metric through kda_intra_bwd_host with pinned host buffers (every step copies
+    the inputs up and the outputs down), and beside it the same bytes copied alone, up
+    and down at once on two streams: the ceiling the host link sets on this machine."""
+    names = ("q", "k", "g", "beta", "dAqk", "dAkk")
+    pin = {n: v.pin_memory() for n, v in cpu.items()}
+    hout = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
+    ws = torch.empty(kda.kda_intra_bwd_host_workspace_bytes(cfg.B, cfg.T, cfg.H, cfg.qk_dtype),
+                     dtype=torch.uint8, device=dev)
+    hin = [pin[n] for n in names]
+    for _ in range(2):
+        kda.kda_intra_bwd_host(*hin, *hout, workspace=ws, stream=stream)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        kda.kda_intra_bwd_host(*hin, *hout, workspace=ws, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+
+    # the link alone: device views of the workspace, inputs then outputs
+    views, off = [], 0
+    for h in hin + hout:
+        nb = h.numel() * h.element_size()
+        views.append(ws[off:off + nb].view(h.dtype).view(h.shape))
+        off += (nb + 255) // 256 * 256
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def copies():
+        start = torch.cuda.Event()
+        start.record(stream)
+        up.wait_event(start)
+        down.wait_event(start)
+        with torch.cuda.stream(up):
+            for h, d in zip(hin, views[:len(hin)]):
+                d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(down):
+            for h, d in zip(hout, views[len(hin):]):
+                h.copy_(d, non_blocking=True)
+        stream.wait_stream(up)
+        stream.wait_stream(down)
+
+    copies()
+    torch.cuda.synchronize(dev)
+    l0 = torch.cuda.Event(enable_timing=True)
+    l1 = torch.cuda.Event(enable_timing=True)
+    l0.record(stream)
+    for _ in range(args.e2e_steps):
+        copies()
+    l1.record(stream)
+    torch.cuda.synchronize(dev)
+    link_ms = max_over_ranks(l0.elapsed_time(l1), world, dev)
+    bi = sum(t.numel() * t.element_size() for t in hin)
+    bo = sum(t.numel() * t.element_size() for t in hout)
+    del ws
+    return {"value": world * cfg.tokens_heads * args.e2e_steps / (e_ms / 1e3),
+            "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "steps": args.e2e_steps, "ms_per_step": e_ms / args.e2e_steps,
+            "entry_point": "kda_intra_bwd_host (pinned host buffers)",
+            "link_ms_per_step": link_ms / args.e2e_steps,
+            "link_gbs": (bi + bo) / (link_ms / args.e2e_steps / 1e3) / 1e9,
+            "link_frac": link_ms / e_ms,
+            "link_how": "the same bytes copied alone (pinned, torch copies), inputs up and "
+                        "outputs down at once on two streams, no kernel"}
+
+
+
 def run_ours(args, cfg):
     world, rank, local = setup_dist()
     import gated_delta_rule_intra_gb300 as kda
@@ -419,6 +560,13 @@ def run_ours(args, cfg):
         def step():
             fn(*ins, *outs, stream=stream)
 
+    qk_bytes = torch.tensor([], dtype=cfg.qk_dtype).element_size()
+    bytes_per_launch = launch_bytes(args, cfg, qk_bytes, fwd)
+    # a working set that fits in the L2 would be served from it by back-to-back steps:
+    # such workloads are timed call by call, each after a write that evicts the L2
+    flushed = bytes_per_launch < 2 * L2_BYTES
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flushed else None
+
     for _ in range(args.warmup):
         step()
     sampler = ClockSampler(device_selector(dev))
@@ -429,49 +577,53 @@ def run_ours(args, cfg):
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     t0 = time.monotonic()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
+    if flushed:
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)]
+        for a, b in pairs:
+            flush.zero_()
+            a.record(stream)
+            step()
+            b.record(stream)
+    else:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
     torch.cuda.synchronize(dev)
     t1 = time.monotonic()
     barrier(world)
     sampler.window = (t0, t1)
     time.sleep(0.25)
     sampler.stop()
-    ms = ev0.elapsed_time(ev1)
+    if flushed:
+        per_call = sorted(a.elapsed_time(b) for a, b in pairs)
+        ms = sum(per_call)
+    else:
+        ms = ev0.elapsed_time(ev1)
     ms_max = max_over_ranks(ms, world, dev)
     ms_per_step = ms_max / args.steps
+
+    host = None
+    if flushed and rank == 0:
+        c_call = None
+        if not extended:  # the C entry point itself, arguments built once
+            import ctypes
+            lib = kda.load_library()
+            vp = ctypes.c_void_p
+            c_fn = getattr(lib, args.path)
+            c_args = ([vp(t.data_ptr()) for t in (ins[:4] if fwd else ins)]
+                      + [vp(t.data_ptr()) for t in outs]
+                      + [cfg.B, cfg.T, cfg.H, kda._DTYPES[cfg.qk_dtype], vp(stream.cuda_stream)])
+            c_call = lambda: c_fn(*c_args)  # noqa: E731
+        host = host_cost(step, c_call, dev)
+        host["device_ms_per_call"] = {"median": per_call[len(per_call) // 2],
+                                      "min": per_call[0], "max": per_call[-1]}
 
     # end to end through the host-buffer entry point
     e2e = None
     if not args.no_e2e and not extended and not fwd:
-        pin = {n: v.pin_memory() for n, v in cpu.items()}
-        hout = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
-        ws = torch.empty(kda.kda_intra_bwd_host_workspace_bytes(cfg.B, cfg.T, cfg.H,
-                                                                 cfg.qk_dtype),
-                         dtype=torch.uint8, device=dev)
-        hin = [pin[n] for n in ("q", "k", "g", "beta", "dAqk", "dAkk")]
-        for _ in range(2):
-            kda.kda_intra_bwd_host(*hin, *hout, workspace=ws, stream=stream)
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            kda.kda_intra_bwd_host(*hin, *hout, workspace=ws, stream=stream)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier(world)
-        e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-        e2e = {"value": world * cfg.tokens_heads * args.e2e_steps / (e_ms / 1e3),
-               "unit": UNIT,
-               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
-               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout),
-               "steps": args.e2e_steps,
-               "entry_point": "kda_intra_bwd_host (pinned host buffers)"}
-        del ws
+        e2e = end_to_end(kda, args, cfg, cpu, outs, stream, dev, world)
 
     cpu_base = None
     if world == 1 and rank == 0 and not args.no_cpu_baseline and not extended and not fwd:
@@ -480,22 +632,10 @@ def run_ours(args, cfg):
 
     if rank != 0:
         return
-    qk_bytes = torch.tensor([], dtype=cfg.qk_dtype).element_size()
-    if fwd:
-        # per valid token row and head: q, k, g, beta in; both 64-column rows out
-        per_row = 2 * kda_inputs.K * qk_bytes / args.gva + kda_inputs.K * 4 + 4 + 2 * 64 * 4
-        rows = cfg.T * cfg.B if args.varlen else cfg.units * kda_inputs.BT / cfg.H
-        bytes_per_launch = rows * cfg.H * per_row
-    elif args.varlen:
-        bytes_per_launch = varlen_algorithmic_bytes(cfg.lens, cfg.H, qk_bytes,
-                                                    accumulate=args.accumulate,
-                                                    io_out=args.io_dtype_out)
-        if args.gva > 1:
-            bytes_per_launch -= cfg.T * cfg.H * 2 * kda_inputs.K * qk_bytes * (1 - 1 / args.gva)
-    else:
-        bytes_per_launch = cfg.units * algorithmic_bytes_per_unit(
-            qk_bytes, group=args.gva, accumulate=args.accumulate, io_out=args.io_dtype_out)
     achieved = bytes_per_launch / (ms / args.steps / 1e3) / 1e9
+    clocks = sampler.summary()
+    if clocks:  # time x clock: a step's length in SM cycles at the sampled clock
+        clocks["kcycles_per_step"] = ms_per_step * clocks["sm_mhz"]
     peak, peak_kind = hbm_peak()
     kname = KERNEL_NAMES[args.path]
     # the committed summaries cover the plain launch of each path only
@@ -509,17 +649,20 @@ def run_ours(args, cfg):
         "vs_baseline": None, "dtype": "f32" if args.path.endswith("fp32") else "tf32+f32",
         "data": "synthetic",
         "config": config_dict(cfg, args.path if fwd else
-                              "kda_intra_bwd_ex" if extended else args.path, opts),
+                              "kda_intra_bwd_ex" if extended else args.path, opts,
+                              flushed=flushed),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     if peak_kind == "measured" else "fallback: nominal 8 TB/s",
                      "kernel": kname, "algorithmic_bytes_per_launch": bytes_per_launch},
         "cpu_baseline": cpu_base,
-        "clocks": sampler.summary(),
+        "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": args.steps,
     }
+    if host is not None:
+        line["host"] = host
     print(json.dumps(line), flush=True)
 
 
@@ -530,9 +673,11 @@ def main():
     p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    p.add_argument("--config", type=int, default=kda_inputs.HEADLINE,
-                   help="index into kda_inputs.CONFIGS (default: the headline workload, "
-                        "B=8 T=4096 H=16)")
+    p.add_argument("--config", default=str(kda_inputs.HEADLINE),
+                   help="workload: an index into kda_inputs.CONFIGS, a short name "
+                        "(single_chunk, small, headline, long, gate_stress), a workload "
+                        "name, or 'all' for one JSON line per workload (default: the "
+                        "headline workload, B=8 T=4096 H=16)")
     p.add_argument("--path", choices=tuple(KERNEL_NAMES), default="kda_intra_bwd")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-e2e", action="store_true")
@@ -553,11 +698,14 @@ def main():
                         "(kda_intra_bwd_ex)")
     args = p.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
-    cfg = kda_inputs.CONFIGS[args.config]
-    if args.impl == "reference":
-        run_reference(args, cfg)
-    else:
-        run_ours(args, cfg)
+    for idx in parse_configs(args.config):
+        args.config = idx
+        cfg = kda_inputs.CONFIGS[idx]
+        if args.impl == "reference":
+            run_reference(args, cfg)
+        else:
+            run_ours(args, cfg)
+            torch.cuda.empty_cache()
 
 
 if __name__ == "__main__":

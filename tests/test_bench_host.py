@@ -46,3 +46,26 @@ def test_traffic_is_null_when_the_summary_is_for_other_sources(monkeypatch):
     assert current > 0.9 * kda_inputs.CONFIGS[kda_inputs.HEADLINE].units * bench.algorithmic_bytes_per_unit()
     monkeypatch.setattr(bench, "source_hash", lambda kernel: "0" * 16)
     assert bench.ncu_traffic(name, workload) is None
+
+
+def test_config_selection():
+    assert bench.parse_configs("2") == [kda_inputs.HEADLINE]
+    assert bench.parse_configs("gate_stress") == [kda_inputs.GATE_STRESS]
+    assert bench.parse_configs("long_B1_T32768_H32") == [kda_inputs.LONG]
+    assert bench.parse_configs("all") == list(range(len(kda_inputs.CONFIGS)))
+    for bad in ("9", "-1", "nope"):
+        with pytest.raises(ValueError):
+            bench.parse_configs(bad)
+
+
+def test_small_workloads_are_timed_with_an_l2_flush():
+    """The single-chunk and small workloads fit in the L2 and are flushed between calls;
+    the others exceed twice the L2 and run back to back."""
+    import types
+    args = types.SimpleNamespace(gva=1, varlen=False, accumulate=False, io_dtype_out=False)
+    fits = [bench.launch_bytes(args, c, 2, False) < 2 * bench.L2_BYTES for c in kda_inputs.CONFIGS]
+    assert fits == [True, True, False, False, False]
+
+
+def test_fallback_peak_is_the_nominal_hbm_rate():
+    assert bench.FALLBACK_HBM_GBS == 8000.0
