@@ -56,8 +56,11 @@ kda_intra_bwd_fp32_kernel(const __grid_constant__ TmaMaps tm, const float *__res
         tc::prefetch_tmap(&tm.q);
         tc::prefetch_tmap(&tm.k);
         tc::prefetch_tmap(&tm.g);
-        tc::prefetch_tmap(&tm.daqk);
-        tc::prefetch_tmap(&tm.dakk);
+#pragma unroll
+        for (int t = 0; t < NBLK; ++t) {
+            tc::prefetch_tmap(&tm.daqk[t]);
+            tc::prefetch_tmap(&tm.dakk[t]);
+        }
     }
     __syncthreads();
     if (warp == 0) {  // the first two units of this CTA

@@ -68,30 +68,35 @@ cudaError_t make_maps(const BwdArgs &a, TmaMaps *tm) {
     // no L2 promotion for dA: a promoted fetch would also pull the rows' unused upper part
     const CUtensorMapL2promotion l2 = CU_TENSOR_MAP_L2_PROMOTION_NONE;
     if (!a.cu_seqlens) {
-        // dA: (col%4, row%8, row/8, col/4, head); one box = one 16x16 block laid out as a
-        // tensor-core operand (4 floats, 8 rows, 2 row groups, 4 column chunks)
+        // dA: (col%4, row%8, row/8, col/4, head); the box of row-block t covers its blocks
+        // (t, 0..t) and lands them as tensor-core operands (4 floats, 8 rows, 2 row groups,
+        // then column chunks: block j at j KB)
         const cuuint64_t dims[5] = {4, 8, rows / 8, BT / 4, H};
         const cuuint64_t str[4] = {H * BT * 4, 8 * H * BT * 4, 16, BT * 4};
-        const cuuint32_t box[5] = {4, 8, 2, 4, 1};
-        if ((e = encode(&tm->daqk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, a.dAqk, dims, str, box,
-                        l2)) != cudaSuccess)
-            return e;
-        if ((e = encode(&tm->dakk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, a.dAkk, dims, str, box,
-                        l2)) != cudaSuccess)
-            return e;
+        for (int t = 0; t < NBLK; ++t) {
+            const cuuint32_t box[5] = {4, 8, 2, (cuuint32_t)(4 * (t + 1)), 1};
+            if ((e = encode(&tm->daqk[t], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, a.dAqk, dims, str,
+                            box, l2)) != cudaSuccess)
+                return e;
+            if ((e = encode(&tm->dakk[t], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, a.dAkk, dims, str,
+                            box, l2)) != cudaSuccess)
+                return e;
+        }
     } else {
         // variable-length units start at any row: (col%4, row, col/4, head), box
-        // (4, 16, 4, 1) -- the same bytes in the same operand layout (row n of the block
-        // at n*16 bytes inside each 256-byte column chunk)
+        // (4, 16, 4(t+1), 1) -- the same bytes in the same operand layout (row n of a
+        // block at n*16 bytes inside each 256-byte column chunk)
         const cuuint64_t dims[4] = {4, rows, BT / 4, H};
         const cuuint64_t str[3] = {H * BT * 4, 16, BT * 4};
-        const cuuint32_t box[4] = {4, BC, 4, 1};
-        if ((e = encode(&tm->daqk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.dAqk, dims, str, box,
-                        l2)) != cudaSuccess)
-            return e;
-        if ((e = encode(&tm->dakk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.dAkk, dims, str, box,
-                        l2)) != cudaSuccess)
-            return e;
+        for (int t = 0; t < NBLK; ++t) {
+            const cuuint32_t box[4] = {4, BC, (cuuint32_t)(4 * (t + 1)), 1};
+            if ((e = encode(&tm->daqk[t], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.dAqk, dims, str,
+                            box, l2)) != cudaSuccess)
+                return e;
+            if ((e = encode(&tm->dakk[t], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.dAkk, dims, str,
+                            box, l2)) != cudaSuccess)
+                return e;
+        }
     }
     return cudaSuccess;
 }

@@ -109,8 +109,10 @@ constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t SPIN_LIMIT = 1u << 22;
 
+// q, k, g: one unit's [64 x 128] tile.  daqk[t], dakk[t]: row-block t's lower blocks
+// (t, 0..t) in one box of 16 rows x 16(t+1) columns, landing in the operand layout.
 struct TmaMaps {
-    CUtensorMap q, k, g, daqk, dakk;
+    CUtensorMap q, k, g, daqk[NBLK], dakk[NBLK];
 };
 
 // Options of the extended entry point.  H in the kernel is the number of heads of g,
@@ -176,7 +178,7 @@ __device__ __forceinline__ void cp_async4_zfill(void *smem, const void *gmem, bo
                  : "memory");
 }
 
-// One warp queues every copy of one unit into a stage: 23 TMA tiles from lane 0,
+// One warp queues every copy of one unit into a stage: 11 TMA tiles from lane 0,
 // beta as 64 four-byte copies from all lanes (its rows are H floats apart, so no
 // tensor map can describe it when H is not a multiple of 4).  A variable-length unit
 // may start at any token row: its dA tiles come through the 4-d map (any row start),
@@ -221,22 +223,18 @@ __device__ __forceinline__ void load_unit(unsigned char *st, uint64_t *full, int
         tc::tma_load_3d(st + ST_Q, &tm.q, 0, h / ex.G, row, full);
         tc::tma_load_3d(st + ST_K, &tm.k, 0, h / ex.G, row, full);
         tc::tma_load_3d(st + ST_G, &tm.g, 0, h, row, full);
+        // row-block t's blocks (t, 0..t) are contiguous in the stage: one box each
 #pragma unroll
         for (int t = 0; t < NBLK; ++t) {
-#pragma unroll
-            for (int j = 0; j <= t; ++j) {
-                if constexpr (VARLEN) {
-                    tc::tma_load_4d(st + ST_DQ + dablk(t, j) * 1024, &tm.daqk, 0, row + BC * t,
-                                    4 * j, h, full);
-                    tc::tma_load_4d(st + ST_DK + dablk(t, j) * 1024, &tm.dakk, 0, row + BC * t,
-                                    4 * j, h, full);
-                } else {
-                    const int rg = (row + BC * t) >> 3;
-                    tc::tma_load_5d(st + ST_DQ + dablk(t, j) * 1024, &tm.daqk, 0, 0, rg, 4 * j,
-                                    h, full);
-                    tc::tma_load_5d(st + ST_DK + dablk(t, j) * 1024, &tm.dakk, 0, 0, rg, 4 * j,
-                                    h, full);
-                }
+            if constexpr (VARLEN) {
+                tc::tma_load_4d(st + ST_DQ + dablk(t, 0) * 1024, &tm.daqk[t], 0, row + BC * t, 0,
+                                h, full);
+                tc::tma_load_4d(st + ST_DK + dablk(t, 0) * 1024, &tm.dakk[t], 0, row + BC * t, 0,
+                                h, full);
+            } else {
+                const int rg = (row + BC * t) >> 3;
+                tc::tma_load_5d(st + ST_DQ + dablk(t, 0) * 1024, &tm.daqk[t], 0, 0, rg, 0, h, full);
+                tc::tma_load_5d(st + ST_DK + dablk(t, 0) * 1024, &tm.dakk[t], 0, 0, rg, 0, h, full);
             }
         }
     }
@@ -297,8 +295,11 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         tc::prefetch_tmap(&tm.q);
         tc::prefetch_tmap(&tm.k);
         tc::prefetch_tmap(&tm.g);
-        tc::prefetch_tmap(&tm.daqk);
-        tc::prefetch_tmap(&tm.dakk);
+#pragma unroll
+        for (int t = 0; t < NBLK; ++t) {
+            tc::prefetch_tmap(&tm.daqk[t]);
+            tc::prefetch_tmap(&tm.dakk[t]);
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
