@@ -25,7 +25,11 @@ BUILD_DIR = os.path.join(PKG, "_build")
 DEBUG_BUILD_DIR = os.path.join(PKG, "_build_debug")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# Hidden visibility: only the C ABI (kda_api.cu) is exported.  Two builds loaded in one
+# process (libkda.so and libkda_debug.so) then share no C++ internals; in particular no
+# function-local static of a template becomes a process-wide unique symbol.
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
+              "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
 
 

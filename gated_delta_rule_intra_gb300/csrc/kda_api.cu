@@ -6,8 +6,12 @@
 
 #include <cuda_runtime.h>
 
-#include "kda.h"
 #include "kda_launch.h"
+
+// The library is built with hidden visibility; the C ABI declared in kda.h is exported.
+#pragma GCC visibility push(default)
+#include "kda.h"
+#pragma GCC visibility pop
 
 namespace {
 

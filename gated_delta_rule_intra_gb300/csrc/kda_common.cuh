@@ -13,6 +13,20 @@ constexpr int BC = 16;        // sub-block length
 constexpr int KD = 128;       // head dimension
 constexpr int NBLK = BT / BC; // 4 sub-blocks per chunk
 constexpr float LN2 = 0.693147180559945309417232121458f;
+constexpr int kMaxDev = 64;   // devices whose per-device launch state is cached
+
+// Raise a kernel's dynamic shared-memory limit once per device (the attribute belongs
+// to the device's copy of the function); `done` is the kernel's own per-device flag
+// array.  Two threads racing here set the same value twice, which is harmless.
+template <typename Kernel>
+cudaError_t smem_limit_once(Kernel kern, int bytes, int dev, volatile int *done) {
+    const bool cached = dev >= 0 && dev < kMaxDev;
+    if (cached && done[dev]) return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && cached) done[dev] = 1;
+    return e;
+}
 
 // 2^x on the SFU (MUFU.EX2), flush-to-zero.  Every argument passed here is <= 0 for
 // inputs inside the method's premise (non-increasing chunk-local gate), so the

@@ -301,10 +301,11 @@ kda_intra_bwd_fp32_kernel(const __grid_constant__ TmaMaps tm, const float *__res
 template <typename io_t>
 cudaError_t launch_typed(const BwdArgs &a, cudaStream_t stream) {
     auto kern = kda_intra_bwd_fp32_kernel<io_t>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, F_TOTAL);
+    static volatile int smem_set[kMaxDev];
+    int nsm = 0, dev = 0;
+    cudaError_t e = num_sms(&nsm, &dev);
     if (e != cudaSuccess) return e;
-    int nsm = 0;
-    if ((e = num_sms(&nsm)) != cudaSuccess) return e;
+    if ((e = smem_limit_once(kern, F_TOTAL, dev, smem_set)) != cudaSuccess) return e;
     TmaMaps tm;
     if ((e = make_maps(a, &tm)) != cudaSuccess) return e;
     Extras ex = {};

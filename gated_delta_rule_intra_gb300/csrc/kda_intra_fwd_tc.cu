@@ -579,7 +579,7 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
 // ---------------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-int g_num_sms[64];
+int g_num_sms[kMaxDev];
 
 cudaError_t get_encoder() {
     if (g_encode) return cudaSuccess;
@@ -606,33 +606,62 @@ cudaError_t encode_rows(CUtensorMap *m, CUtensorMapDataType dt, int esize, const
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <typename io_t, bool VARLEN>
-cudaError_t launch_typed(const FwdArgs &a, cudaStream_t stream) {
-    auto kern = kda_intra_fwd_tc_kernel<io_t, VARLEN>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         FM_ALLOC);
-    if (e != cudaSuccess) return e;
-    if ((e = get_encoder()) != cudaSuccess) return e;
-    int dev = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    int nsm = (dev >= 0 && dev < 64) ? g_num_sms[dev] : 0;
-    if (nsm == 0) {
-        if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-            return e;
-        if (dev >= 0 && dev < 64) g_num_sms[dev] = nsm;
+// What a set of forward tensor maps depends on (a map is a pure function of these):
+// the maps of a thread's previous call are reused when the key is the same.
+struct FwdKey {
+    const void *q, *k, *g, *Aqk, *Akk;
+    int B, T, H, HV;
+    bool fp16;
+    bool operator==(const FwdKey &o) const {
+        return q == o.q && k == o.k && g == o.g && Aqk == o.Aqk && Akk == o.Akk && B == o.B &&
+               T == o.T && H == o.H && HV == o.HV && fp16 == o.fp16;
     }
-    const int HV = a.HV > 0 ? a.HV : a.H;
+};
+thread_local FwdKey t_key;
+thread_local FwdMaps t_maps;
+thread_local bool t_valid = false;
+
+cudaError_t fwd_maps(const FwdArgs &a, int HV, FwdMaps *tm) {
+    const FwdKey key = {a.q, a.k, a.g, a.Aqk, a.Akk, a.B, a.T, a.H, HV, a.fp16};
+    if (t_valid && key == t_key) {
+        *tm = t_maps;
+        return cudaSuccess;
+    }
+    cudaError_t e = get_encoder();
+    if (e != cudaSuccess) return e;
     const cuuint64_t rows = (cuuint64_t)a.B * a.T, HQ = (cuuint64_t)a.H, H = (cuuint64_t)HV;
     const CUtensorMapDataType io =
         a.fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-    FwdMaps tm;
-    if ((e = encode_rows(&tm.q, io, 2, a.q, KD, HQ, rows)) != cudaSuccess ||
-        (e = encode_rows(&tm.k, io, 2, a.k, KD, HQ, rows)) != cudaSuccess ||
-        (e = encode_rows(&tm.g, f32, 4, a.g, KD, H, rows)) != cudaSuccess ||
-        (e = encode_rows(&tm.aqk, f32, 4, a.Aqk, BT, H, rows)) != cudaSuccess ||
-        (e = encode_rows(&tm.akk, f32, 4, a.Akk, BT, H, rows)) != cudaSuccess)
+    if ((e = encode_rows(&tm->q, io, 2, a.q, KD, HQ, rows)) != cudaSuccess ||
+        (e = encode_rows(&tm->k, io, 2, a.k, KD, HQ, rows)) != cudaSuccess ||
+        (e = encode_rows(&tm->g, f32, 4, a.g, KD, H, rows)) != cudaSuccess ||
+        (e = encode_rows(&tm->aqk, f32, 4, a.Aqk, BT, H, rows)) != cudaSuccess ||
+        (e = encode_rows(&tm->akk, f32, 4, a.Akk, BT, H, rows)) != cudaSuccess)
         return e;
+    t_key = key;
+    t_maps = *tm;
+    t_valid = true;
+    return cudaSuccess;
+}
+
+template <typename io_t, bool VARLEN>
+cudaError_t launch_typed(const FwdArgs &a, cudaStream_t stream) {
+    auto kern = kda_intra_fwd_tc_kernel<io_t, VARLEN>;
+    static volatile int smem_set[kMaxDev];  // this instantiation's attribute, per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = smem_limit_once(kern, FM_ALLOC, dev, smem_set)) != cudaSuccess) return e;
+    int nsm = (dev >= 0 && dev < kMaxDev) ? g_num_sms[dev] : 0;
+    if (nsm == 0) {
+        if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return e;
+        if (dev >= 0 && dev < kMaxDev) g_num_sms[dev] = nsm;
+    }
+    const int HV = a.HV > 0 ? a.HV : a.H;
+    FwdMaps tm;
+    if ((e = fwd_maps(a, HV, &tm)) != cudaSuccess) return e;
     FwdExtras ex;
     ex.G = HV / a.H;
     ex.cu_seqlens = a.cu_seqlens;

@@ -16,7 +16,7 @@ cudaError_t launch_tc_fp16_varlen_fd(const BwdArgs &a, cudaStream_t stream);
 
 namespace tcimpl {
 namespace {
-int g_num_sms[64];
+int g_num_sms[kMaxDev];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 cudaError_t get_encoder() {
@@ -43,7 +43,46 @@ cudaError_t encode(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void 
 
 }  // namespace
 
+namespace {
+
+// What a set of tensor maps depends on.  A map is a pure function of these, so a set
+// encoded once serves every later call with the same key (the host's per-call cost).
+struct MapKey {
+    const void *q, *k, *g, *dAqk, *dAkk;
+    int B, T, H, HV;
+    bool fp16, varlen;
+    bool operator==(const MapKey &o) const {
+        return q == o.q && k == o.k && g == o.g && dAqk == o.dAqk && dAkk == o.dAkk &&
+               B == o.B && T == o.T && H == o.H && HV == o.HV && fp16 == o.fp16 &&
+               varlen == o.varlen;
+    }
+};
+thread_local MapKey t_key;
+thread_local TmaMaps t_maps;
+thread_local bool t_valid = false;
+
+cudaError_t encode_maps(const BwdArgs &a, TmaMaps *tm);
+
+}  // namespace
+
 cudaError_t make_maps(const BwdArgs &a, TmaMaps *tm) {
+    const MapKey key = {a.q, a.k, a.g, a.dAqk, a.dAkk, a.B, a.T, a.H,
+                        a.HV > 0 ? a.HV : a.H, a.fp16, a.cu_seqlens != nullptr};
+    if (t_valid && key == t_key) {
+        *tm = t_maps;
+        return cudaSuccess;
+    }
+    const cudaError_t e = encode_maps(a, tm);
+    if (e != cudaSuccess) return e;
+    t_key = key;
+    t_maps = *tm;
+    t_valid = true;
+    return cudaSuccess;
+}
+
+namespace {
+
+cudaError_t encode_maps(const BwdArgs &a, TmaMaps *tm) {
     cudaError_t e = get_encoder();
     if (e != cudaSuccess) return e;
     const cuuint64_t rows = (cuuint64_t)a.B * a.T, HQ = (cuuint64_t)a.H;
@@ -101,17 +140,20 @@ cudaError_t make_maps(const BwdArgs &a, TmaMaps *tm) {
     return cudaSuccess;
 }
 
-cudaError_t num_sms(int *n) {
+}  // namespace
+
+cudaError_t num_sms(int *n, int *devp) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int v = (dev >= 0 && dev < 64) ? g_num_sms[dev] : 0;
+    int v = (dev >= 0 && dev < kMaxDev) ? g_num_sms[dev] : 0;
     if (v == 0) {
         if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return e;
-        if (dev >= 0 && dev < 64) g_num_sms[dev] = v;
+        if (dev >= 0 && dev < kMaxDev) g_num_sms[dev] = v;
     }
     *n = v;
+    *devp = dev;
     return cudaSuccess;
 }
 

@@ -911,19 +911,20 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
 
 // ---------------------------------------------------------------- host side
 
-// Defined once in kda_intra_tc.cu.
+// Defined once in kda_intra_tc.cu.  make_maps reuses the maps of its thread's previous
+// call when the pointers and shapes are the same; num_sms also returns the device.
 cudaError_t make_maps(const BwdArgs &a, TmaMaps *tm);
-cudaError_t num_sms(int *n);
+cudaError_t num_sms(int *n, int *dev);
 
 template <typename io_t, bool ACCUM, bool FOLD, bool EMIT, bool VARLEN, bool FACTOR>
 cudaError_t launch_typed(const BwdArgs &a, cudaStream_t stream) {
     auto kern = kda_intra_bwd_tc_kernel<io_t, ACCUM, FOLD, EMIT, VARLEN, FACTOR>;
     const int smem_bytes = FOLD ? SM_TOTAL_FOLD : SM_TOTAL;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    static volatile int smem_set[kMaxDev];  // this instantiation's attribute, per device
+    int nsm = 0, dev = 0;
+    cudaError_t e = num_sms(&nsm, &dev);
     if (e != cudaSuccess) return e;
-    int nsm = 0;
-    if ((e = num_sms(&nsm)) != cudaSuccess) return e;
+    if ((e = smem_limit_once(kern, smem_bytes, dev, smem_set)) != cudaSuccess) return e;
     TmaMaps tm;
     if ((e = make_maps(a, &tm)) != cudaSuccess) return e;
     const int HV = a.HV > 0 ? a.HV : a.H;
