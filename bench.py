@@ -547,10 +547,11 @@ def run_ours(args, cfg):
     ins = [x[n] for n in ("q", "k", "g", "beta", "dAqk", "dAkk")]
     fwd = args.path == "kda_intra_fwd"
     extended = (args.gva > 1 or args.accumulate or args.fold_dg or args.io_dtype_out
-                or args.varlen or args.factor_diag)
+                or args.varlen or args.factor_diag or args.split_tf32)
     opts = None
     if fwd:
-        if args.accumulate or args.fold_dg or args.io_dtype_out or args.factor_diag:
+        if (args.accumulate or args.fold_dg or args.io_dtype_out or args.factor_diag
+                or args.split_tf32):
             raise SystemExit("the forward takes --gva and --varlen only")
         outs = list(kda.kda_intra_fwd(*ins[:4], **varlen))
         if extended:
@@ -569,11 +570,13 @@ def run_ours(args, cfg):
                           for n in ("dq_in", "dk_in", "dg_in")})
             extra["db_in"] = torch.randn(cfg.B, cfg.T, cfg.H, generator=gen).to(dev)
         extra["factor_diag"] = args.factor_diag
+        extra["split_tf32"] = args.split_tf32
         outs = list(kda.kda_intra_bwd_ex(*ins, **extra, fold_dg=args.fold_dg,
                                          dqdk_io_dtype=args.io_dtype_out))
         opts = {"value_heads_per_qk_head": args.gva, "accumulate": args.accumulate,
                 "fold_dg": args.fold_dg, "dqdk_io_dtype": args.io_dtype_out,
-                "varlen": args.varlen, "factor_diag": args.factor_diag}
+                "varlen": args.varlen, "factor_diag": args.factor_diag,
+                "split_tf32": args.split_tf32}
 
         def step():
             kda.kda_intra_bwd_ex(*ins, *outs, **extra, fold_dg=args.fold_dg,
@@ -671,7 +674,9 @@ def run_ours(args, cfg):
         "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32" if args.path.endswith("fp32") else "tf32+f32",
+        "vs_baseline": None,
+        "dtype": "f32" if args.path.endswith("fp32") else
+                 "split-tf32+f32" if args.split_tf32 else "tf32+f32",
         "data": "synthetic",
         "config": config_dict(cfg, args.path if fwd else
                               "kda_intra_bwd_ex" if extended else args.path, opts,
@@ -721,6 +726,8 @@ def main():
     p.add_argument("--factor-diag", action="store_true",
                    help="diagonal blocks' lower-left quadrant factorized through row 8 "
                         "(kda_intra_bwd_ex)")
+    p.add_argument("--split-tf32", action="store_true",
+                   help="cross sums in split TF32, FP32-level accuracy (kda_intra_bwd_ex)")
     args = p.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     for idx in parse_configs(args.config):

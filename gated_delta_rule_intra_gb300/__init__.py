@@ -11,7 +11,8 @@ The functions carry the C names of ``include/kda.h``:
 * ``kda_intra_bwd_ex``    -- fast path with options: grouped value heads, incoming
   gradients added in-kernel, dg folded to its chunk-local reverse cumsum, dq/dk in
   the q/k dtype, variable-length sequences (``cu_seqlens``), the diagonal quadrant
-  factorized (``factor_diag``)
+  factorized (``factor_diag``), the cross sums in split TF32 for FP32-level accuracy
+  (``split_tf32``)
 * ``prepare_chunk_indices`` -- the (sequence, chunk) table of a ``cu_seqlens``
 * ``kda_intra_bwd_host``  -- host buffers in and out, copies on the stream
 * ``kda_intra_bwd_host_static`` -- the same without a workspace, staged in the library's
@@ -37,7 +38,7 @@ DEBUG_LIB_PATH = os.path.join(_HERE, "libkda_debug.so")
 
 # KDA_ABI_VERSION of the include/kda.h these ctypes mirrors follow (option structs,
 # signatures); a library of any other version is refused at load.
-ABI_VERSION = 8
+ABI_VERSION = 9
 KDA_OK = 0
 KDA_BF16 = 0
 KDA_FP16 = 1
@@ -57,7 +58,7 @@ class KdaOpts(ctypes.Structure):
                 ("fold_dg", ctypes.c_int), ("dqdk_io_dtype", ctypes.c_int),
                 ("cu_seqlens", ctypes.c_void_p), ("chunk_indices", ctypes.c_void_p),
                 ("num_seqs", ctypes.c_int), ("num_chunks", ctypes.c_int),
-                ("factor_diag", ctypes.c_int)]
+                ("factor_diag", ctypes.c_int), ("split_tf32", ctypes.c_int)]
 
 
 class KdaFwdOpts(ctypes.Structure):
@@ -267,7 +268,7 @@ def prepare_chunk_indices(cu_seqlens, bt: int = BT):
 def kda_intra_bwd_ex(q, k, g, beta, dAqk, dAkk, dq=None, dk=None, db=None, dg=None, *,
                      dq_in=None, dk_in=None, dg_in=None, db_in=None, fold_dg=False,
                      dqdk_io_dtype=False, cu_seqlens=None, chunk_indices=None,
-                     factor_diag=False, stream=None):
+                     factor_diag=False, split_tf32=False, stream=None):
     """Intra-chunk backward with the extended options of ``kda_intra_bwd_ex``.
 
     q, k have H heads; g, beta, dAqk, dAkk, the outputs and the optional incoming
@@ -280,7 +281,9 @@ def kda_intra_bwd_ex(q, k, g, beta, dAqk, dAkk, dq=None, dk=None, db=None, dg=No
     ``prepare_chunk_indices(cu_seqlens)``, which reads cu_seqlens on the host.
     ``factor_diag`` factorizes the lower-left 8x8 quadrant of each diagonal 16x16 block
     through the block's row 8 (every exponent stays <= 0) instead of one exp2 per
-    (r, s, d); faster, equal up to rounding.
+    (r, s, d); faster, equal up to rounding.  ``split_tf32`` takes the cross-sub-block
+    sums in split TF32 (three tensor-core products per term) for FP32-level accuracy
+    (1e-4), with no other option but grouped value heads.
     Returns (dq, dk, db, dg).
     """
     if q.device.type != "cuda":
@@ -317,6 +320,7 @@ def kda_intra_bwd_ex(q, k, g, beta, dAqk, dAkk, dq=None, dk=None, db=None, dg=No
     opts.fold_dg = int(bool(fold_dg))
     opts.dqdk_io_dtype = int(bool(dqdk_io_dtype))
     opts.factor_diag = int(bool(factor_diag))
+    opts.split_tf32 = int(bool(split_tf32))
     _varlen_opts(opts, cu_seqlens, chunk_indices, dev)
     lib = load_library()
     ptr = ctypes.c_void_p

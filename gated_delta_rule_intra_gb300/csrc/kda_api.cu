@@ -114,6 +114,10 @@ kda_status_t check_ex(const void *q, const void *k, const float *g, const float 
     if (o.dqdk_io_dtype != 0 && o.dqdk_io_dtype != 1) return KDA_ERR_OPTION;
     if (o.dqdk_io_dtype && HV != H) return KDA_ERR_OPTION;
     if (o.factor_diag != 0 && o.factor_diag != 1) return KDA_ERR_OPTION;
+    if (o.split_tf32 != 0 && o.split_tf32 != 1) return KDA_ERR_OPTION;
+    if (o.split_tf32 && (varlen || o.fold_dg || o.dqdk_io_dtype || o.factor_diag || o.dq_in ||
+                         o.dk_in || o.dg_in || o.db_in))
+        return KDA_ERR_OPTION;
     const void *a16[] = {q, k, g, dAqk, dAkk, dq, dk, dg};
     for (const void *p : a16)
         if ((uintptr_t)p % 16u) return KDA_ERR_ALIGN;
@@ -254,6 +258,7 @@ kda_status_t kda_intra_bwd_ex(const void *q, const void *k, const float *g,
     a.fold_dg = o.fold_dg != 0;
     a.emit_io = o.dqdk_io_dtype != 0;
     a.factor_diag = o.factor_diag != 0;
+    a.split = o.split_tf32 != 0;
     a.cu_seqlens = o.cu_seqlens;
     a.chunk_indices = o.chunk_indices;
     a.num_seqs = o.num_seqs;

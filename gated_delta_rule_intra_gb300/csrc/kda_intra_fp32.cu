@@ -115,7 +115,7 @@ kda_intra_bwd_fp32_kernel(const __grid_constant__ TmaMaps tm, const float *__res
                 const float cj = (j == i - 1) ? 1.f : ex2(g2[0].x - ge);  // 2^(g_16i - g_e(j))
                 const float *bq = daq + dablk(i, j) * 256;
                 const float *bk = dak + dablk(i, j) * 256;
-#pragma unroll 1
+#pragma unroll 2
                 for (int c4 = 0; c4 < 4; ++c4) {
                     float kv[4];
 #pragma unroll
@@ -157,7 +157,7 @@ kda_intra_bwd_fp32_kernel(const __grid_constant__ TmaMaps tm, const float *__res
                 const float cj = (j == i + 1) ? 1.f : ex2(gb - ge);  // 2^(g_16j - g_e(i))
                 const float *bq = daq + dablk(j, i) * 256;
                 const float *bk = dak + dablk(j, i) * 256;
-#pragma unroll 2
+#pragma unroll 4
                 for (int r = 0; r < BC; ++r) {
                     const int rr = BC * j + r;
                     const float f = ex2(sg[rr * KD + d] - gb) * cj;

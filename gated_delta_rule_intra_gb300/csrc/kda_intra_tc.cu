@@ -13,6 +13,8 @@ cudaError_t launch_tc_bf16_fd(const BwdArgs &a, cudaStream_t stream);
 cudaError_t launch_tc_fp16_fd(const BwdArgs &a, cudaStream_t stream);
 cudaError_t launch_tc_bf16_varlen_fd(const BwdArgs &a, cudaStream_t stream);
 cudaError_t launch_tc_fp16_varlen_fd(const BwdArgs &a, cudaStream_t stream);
+cudaError_t launch_tc_bf16_split(const BwdArgs &a, cudaStream_t stream);
+cudaError_t launch_tc_fp16_split(const BwdArgs &a, cudaStream_t stream);
 
 namespace tcimpl {
 namespace {
@@ -160,6 +162,7 @@ cudaError_t num_sms(int *n, int *devp) {
 }  // namespace tcimpl
 
 cudaError_t launch_intra_tc(const BwdArgs &a, cudaStream_t stream) {
+    if (a.split) return a.fp16 ? launch_tc_fp16_split(a, stream) : launch_tc_bf16_split(a, stream);
     if (a.factor_diag) {
         if (a.cu_seqlens)
             return a.fp16 ? launch_tc_fp16_varlen_fd(a, stream)

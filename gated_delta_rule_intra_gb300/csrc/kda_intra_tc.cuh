@@ -80,12 +80,24 @@ constexpr int LUT_BATCH = 32;
 constexpr int SM_TRTAB = SM_LUT + 2 * LUT_BATCH * 8;  // per-thread transpose indices
                                                       // (option instantiations)
 constexpr int SM_TOTAL = SM_TRTAB + 3 * TC_THREADS * 4;
+// extra shared memory of the split-TF32 variant: the low parts of the dA operands, as
+// tensor-core operands in the layouts of their high parts -- the six off-diagonal blocks
+// of each tensor (row-block t's blocks (t, 0..t-1) at block t(t-1)/2 + j, so each target's
+// run is contiguous), then the transposed column-side blocks -- and the barrier and
+// counter of the second MMA pass.
+constexpr int SM_SPLIT_Q = (SM_TOTAL + 1023) / 1024 * 1024;
+constexpr int SM_SPLIT_K = SM_SPLIT_Q + 6144;
+constexpr int SM_SPLIT_CQ = SM_SPLIT_K + 6144;
+constexpr int SM_SPLIT_CK = SM_SPLIT_CQ + 6144;
+constexpr int SM_SPLIT_BAR = SM_SPLIT_CK + 6144;  // pass-2 MMAs-done mbarrier, pass-2 counter
+constexpr int SM_TOTAL_SPLIT = SM_SPLIT_BAR + 16;
 // extra shared memory of the fold_dg variant: the per-row dg bank [64][128] and the
 // per-(sub-block, channel) totals, double-buffered by unit parity
 constexpr int SM_FOLD_BANK = (SM_TOTAL + 127) / 128 * 128;
 constexpr int SM_FOLD_TOT = SM_FOLD_BANK + BT * KD * 4;
 constexpr int SM_TOTAL_FOLD = SM_FOLD_TOT + 2 * NBLK * KD * 4;
 static_assert(STAGE_BYTES % 128 == 0, "TMA destinations need 128-byte alignment");
+static_assert(SM_TOTAL_SPLIT <= 232448 && SM_TOTAL_FOLD <= 232448, "shared memory per CTA");
 static_assert(ST_DQ % 1024 == 0 && ST_DK % 1024 == 0, "dA tiles alignment");
 
 constexpr uint32_t STAGE_TX_BYTES = 2 * BT * KD * 2 + BT * KD * 4 + 2 * 10 * 1024;
@@ -178,6 +190,27 @@ __device__ __forceinline__ void cp_async4_zfill(void *smem, const void *gmem, bo
                  : "memory");
 }
 
+// x rounded to TF32 (10 explicit mantissa bits, round to nearest, ties away), as FP32.
+__device__ __forceinline__ float tf32_rna(float x) {
+    uint32_t y;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
+    return __uint_as_float(y);
+}
+
+// 16 TMEM columns of a TF32 operand: the values themselves, or (SPLIT) their high
+// (LO = false) or low (LO = true) parts.
+template <bool SPLIT, bool LO>
+__device__ __forceinline__ void tmem_st_part(uint32_t taddr, const float (&v)[16]) {
+    if constexpr (SPLIT) {
+        float w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = LO ? v[e] - tf32_rna(v[e]) : tf32_rna(v[e]);
+        tc::tmem_st16(taddr, w);
+    } else {
+        tc::tmem_st16(taddr, v);
+    }
+}
+
 // One warp queues every copy of one unit into a stage: 11 TMA tiles from lane 0,
 // beta as 64 four-byte copies from all lanes (its rows are H floats apart, so no
 // tensor map can describe it when H is not a multiple of 4).  A variable-length unit
@@ -264,7 +297,12 @@ __device__ __forceinline__ void load_unit(unsigned char *st, uint64_t *full, int
 // diagonal-block dA rows read as 0, their gate as the last valid row's (so every
 // exponent stays <= 0), their off-diagonal dA rows are zeroed in the column-side
 // operands, and nothing is stored for them.
-template <typename io_t, bool ACCUM, bool FOLD, bool EMIT, bool VARLEN, bool FACTOR>
+// SPLIT: the cross-sub-block sums in split TF32 for FP32-level accuracy.  Every operand
+// x is cut into hi = tf32(x) (round to nearest) and lo = x - hi (exact in FP32); the
+// tensor core accumulates A_hi B_hi + A_hi B_lo (pass 1) and A_lo B_hi (pass 2, after
+// A_lo replaces A_hi in TMEM), leaving out A_lo B_lo (about 2^-22 of the product).
+template <typename io_t, bool ACCUM, bool FOLD, bool EMIT, bool VARLEN, bool FACTOR,
+          bool SPLIT = false>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restrict__ beta,
                         void *dq_out, void *dk_out, float *db, float *dg, int T, int H,
@@ -285,11 +323,17 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
     float *sdbp = reinterpret_cast<float *>(smem + SM_DBP);
     const long long stride = gridDim.x;
 
+    uint64_t *mbar2 = reinterpret_cast<uint64_t *>(smem + SM_SPLIT_BAR);  // SPLIT only
+    uint32_t *ops2_count = reinterpret_cast<uint32_t *>(smem + SM_SPLIT_BAR + 8);
     if (warp == 0) tc::tmem_alloc(tslot, TM_COLS);
     if (tid == 0) {
         tc::mbar_init(&full[0], FULL_ARRIVALS);
         tc::mbar_init(&full[1], FULL_ARRIVALS);
         tc::mbar_init(mbar, 1);
+        if constexpr (SPLIT) {
+            tc::mbar_init(mbar2, 1);
+            ops2_count[0] = 0u;
+        }
         ops_count[0] = 0u;
         done_count[0] = 0u;
         tc::prefetch_tmap(&tm.q);
@@ -497,7 +541,7 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
                 v[2 * m + 1] = vv.y;
             }
             tc::tmem_st16(tlane + TM_FA + 16 * i, a);
-            tc::tmem_st16(tlane + tm_arow(i + 1) + 16 * i, v);
+            tmem_st_part<SPLIT, false>(tlane + tm_arow(i + 1) + 16 * i, v);
             if (i + 2 < NBLK) {
                 c2 = ex2(gsel(r0 + 2 * BC, sg[(r0 + 2 * BC) * KD + d]) - ge);
 #pragma unroll
@@ -506,7 +550,7 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
                     a[2 * m] = t.x;
                     a[2 * m + 1] = t.y;
                 }
-                tc::tmem_st16(tlane + tm_arow(i + 2) + 16 * i, a);
+                tmem_st_part<SPLIT, false>(tlane + tm_arow(i + 2) + 16 * i, a);
             }
             if (i + 3 < NBLK) {
                 c3 = ex2(gsel(r0 + 3 * BC, sg[(r0 + 3 * BC) * KD + d]) - ge);
@@ -516,7 +560,7 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
                     a[2 * m] = t.x;
                     a[2 * m + 1] = t.y;
                 }
-                tc::tmem_st16(tlane + tm_arow(i + 3) + 16 * i, a);
+                tmem_st_part<SPLIT, false>(tlane + tm_arow(i + 3) + 16 * i, a);
             }
         }
         if (i > 0) {
@@ -537,7 +581,7 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
                 v[2 * m] = t.x;
                 v[2 * m + 1] = t.y;
             }
-            tc::tmem_st16(tlane + TM_AQB + 16 * (i - 1), v);
+            tmem_st_part<SPLIT, false>(tlane + TM_AQB + 16 * (i - 1), v);
 #pragma unroll
             for (int m = 0; m < BC / 2; ++m) {
                 const float2 bk = __fmul2_rn(*reinterpret_cast<const float2 *>(sbeta + r0 + 2 * m), k2[m]);
@@ -545,16 +589,47 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
                 v[2 * m] = t.x;
                 v[2 * m + 1] = t.y;
             }
-            tc::tmem_st16(tlane + TM_AKBB + 16 * (i - 1), v);
+            tmem_st_part<SPLIT, false>(tlane + TM_AKBB + 16 * (i - 1), v);
         }
 
         {
             float *cq = reinterpret_cast<float *>(smem + SM_BCQ);
             float *ck = reinterpret_cast<float *>(smem + SM_BCK);
+            if constexpr (SPLIT) {
+                // this thread is the only one that reads or writes its three elements of
+                // each tensor's off-diagonal blocks: the high parts replace them in the
+                // stage (row-side B operands) and go transposed to the column-side
+                // operands; the low parts go to the same places of the low-part copies
+                float *aq = reinterpret_cast<float *>(st + ST_DQ);
+                float *ak = reinterpret_cast<float *>(st + ST_DK);
+                float *ql = reinterpret_cast<float *>(smem + SM_SPLIT_Q);
+                float *kl = reinterpret_cast<float *>(smem + SM_SPLIT_K);
+                float *cql = reinterpret_cast<float *>(smem + SM_SPLIT_CQ);
+                float *ckl = reinterpret_cast<float *>(smem + SM_SPLIT_CK);
 #pragma unroll
-            for (int x = 0; x < 3; ++x) {
-                cq[trdst[x]] = trq[x];
-                ck[trdst[x]] = trk[x];
+                for (int x = 0; x < 3; ++x) {
+                    int src, dst, row;
+                    tr_index(x, src, dst, row);
+                    const int blk = src >> 8;  // dablk(t, j), j < t
+                    const int t = blk >= 6 ? 3 : blk >= 3 ? 2 : 1;
+                    const int lsrc = ((t * (t - 1) / 2) + (blk - t * (t + 1) / 2)) * 256 + (src & 255);
+                    const float hq = tf32_rna(trq[x]), hk = tf32_rna(trk[x]);
+                    const float lq = trq[x] - hq, lk = trk[x] - hk;
+                    cq[dst] = hq;
+                    ck[dst] = hk;
+                    cql[dst] = lq;
+                    ckl[dst] = lk;
+                    aq[src] = hq;
+                    ak[src] = hk;
+                    ql[lsrc] = lq;
+                    kl[lsrc] = lk;
+                }
+            } else {
+#pragma unroll
+                for (int x = 0; x < 3; ++x) {
+                    cq[trdst[x]] = trq[x];
+                    ck[trdst[x]] = trk[x];
+                }
             }
         }
 
@@ -598,6 +673,34 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
                     for (int kk = 0; kk < 2; ++kk)
                         tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AKBB + 16 * (j - 1) + 8 * kk,
                                         ck0 + ((bcol_off(j) + 256 * kk) >> 4), idj, true);
+                }
+                if constexpr (SPLIT) {  // pass 1, second half: A_hi times the low parts of B
+                    const uint64_t ql0 = tc::smem_desc(tc::smem_u32(smem + SM_SPLIT_Q), 256, 128);
+                    const uint64_t kl0 = tc::smem_desc(tc::smem_u32(smem + SM_SPLIT_K), 256, 128);
+                    const uint64_t cql0 = tc::smem_desc(tc::smem_u32(smem + SM_SPLIT_CQ), 128, 512);
+                    const uint64_t ckl0 = tc::smem_desc(tc::smem_u32(smem + SM_SPLIT_CK), 128, 512);
+#pragma unroll
+                    for (int t = 1; t < NBLK; ++t) {
+#pragma unroll
+                        for (int kk = 0; kk < 2 * t; ++kk) {
+                            const uint32_t a = tbase + tm_arow(t) + 8 * kk;
+                            const uint64_t boff = (uint64_t)(((t * (t - 1) / 2) * 1024 + 512 * kk) >> 4);
+                            tc::mma_tf32_ts(tbase + TM_XQ + 16 * (t - 1), a, ql0 + boff, id16, true);
+                            tc::mma_tf32_ts(tbase + TM_XK + 16 * (t - 1), a, kl0 + boff, id16, true);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 1; j < NBLK; ++j) {
+                        const uint32_t idj = tc::idesc_tf32(128, 16 * j);
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const uint64_t off = (bcol_off(j) + 256 * kk) >> 4;
+                            tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AQB + 16 * (j - 1) + 8 * kk,
+                                            cql0 + off, idj, true);
+                            tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AKBB + 16 * (j - 1) + 8 * kk,
+                                            ckl0 + off, idj, true);
+                        }
+                    }
                 }
                 tc::mma_commit(mbar);
             }
@@ -779,10 +882,115 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         fetch_in(BC - 1);
         fetch_in(BC - 2);
         fetch_in(BC - 3);
+        // SPLIT: rows 15..12, then the second MMA pass is prepared, then rows 11..8
+        constexpr int RMID = SPLIT ? 3 * BC / 4 : BC / 2;
 #pragma unroll
-        for (int r = BC - 1; r >= BC / 2; --r) {
+        for (int r = BC - 1; r >= RMID; --r) {
             if constexpr (!FACTOR) accq[r] = acck[r] = 0.f;
             diag_row(r);
+        }
+        if constexpr (SPLIT) {
+            // pass 1 done: the A operands it read are replaced by their low parts
+            // (recomputed exactly as in the prescale), then the last warp issues pass 2
+            ok &= tc::mbar_wait(mbar, (uint32_t)it & 1u, SPIN_LIMIT);
+            tc::fence_after_sync();
+            if (i < NBLK - 1) {
+                float a[BC], v[BC];
+                tc::tmem_ld16(tlane + TM_FA + 16 * i, a);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int m = 0; m < BC / 2; ++m) {
+                    const float2 vv = __fmul2_rn(k2[m], make_float2(a[2 * m], a[2 * m + 1]));
+                    v[2 * m] = vv.x;
+                    v[2 * m + 1] = vv.y;
+                }
+                tmem_st_part<true, true>(tlane + tm_arow(i + 1) + 16 * i, v);
+                if (i + 2 < NBLK) {
+#pragma unroll
+                    for (int m = 0; m < BC / 2; ++m) {
+                        const float2 t = __fmul2_rn(make_float2(v[2 * m], v[2 * m + 1]), make_float2(c2, c2));
+                        a[2 * m] = t.x;
+                        a[2 * m + 1] = t.y;
+                    }
+                    tmem_st_part<true, true>(tlane + tm_arow(i + 2) + 16 * i, a);
+                }
+                if (i + 3 < NBLK) {
+#pragma unroll
+                    for (int m = 0; m < BC / 2; ++m) {
+                        const float2 t = __fmul2_rn(make_float2(v[2 * m], v[2 * m + 1]), make_float2(c3, c3));
+                        a[2 * m] = t.x;
+                        a[2 * m + 1] = t.y;
+                    }
+                    tmem_st_part<true, true>(tlane + tm_arow(i + 3) + 16 * i, a);
+                }
+            }
+            if (i > 0) {
+                float b[BC], v[BC];
+                tc::tmem_ld16(tlane + TM_FB + 16 * (i - 1), b);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int m = 0; m < BC / 2; ++m) {
+                    const float2 t = __fmul2_rn(make_float2(to_f32(sq[(r0 + 2 * m) * KD + d]),
+                                                            to_f32(sq[(r0 + 2 * m + 1) * KD + d])),
+                                                make_float2(b[2 * m], b[2 * m + 1]));
+                    v[2 * m] = t.x;
+                    v[2 * m + 1] = t.y;
+                }
+                tmem_st_part<true, true>(tlane + TM_AQB + 16 * (i - 1), v);
+#pragma unroll
+                for (int m = 0; m < BC / 2; ++m) {
+                    const float2 bk = __fmul2_rn(*reinterpret_cast<const float2 *>(sbeta + r0 + 2 * m), k2[m]);
+                    const float2 t = __fmul2_rn(bk, make_float2(b[2 * m], b[2 * m + 1]));
+                    v[2 * m] = t.x;
+                    v[2 * m + 1] = t.y;
+                }
+                tmem_st_part<true, true>(tlane + TM_AKBB + 16 * (i - 1), v);
+            }
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            __syncwarp();
+            uint32_t prev2 = 0;
+            if (lane == 0) prev2 = tc::atomic_add_acq_rel_smem(ops2_count, 1u);
+            prev2 = __shfl_sync(0xffffffffu, prev2, 0);
+            if ((prev2 % TC_WARPS) == TC_WARPS - 1) {
+                tc::fence_after_sync();
+                const uint64_t dq0 = tc::smem_desc(tc::smem_u32(st + ST_DQ), 256, 128);
+                const uint64_t dk0 = tc::smem_desc(tc::smem_u32(st + ST_DK), 256, 128);
+                const uint64_t cq0 = tc::smem_desc(tc::smem_u32(smem + SM_BCQ), 128, 512);
+                const uint64_t ck0 = tc::smem_desc(tc::smem_u32(smem + SM_BCK), 128, 512);
+                const uint32_t id16 = tc::idesc_tf32(128, 16);
+                if (tc::elect_one()) {  // pass 2: A_lo times the high parts of B
+#pragma unroll
+                    for (int t = 1; t < NBLK; ++t) {
+#pragma unroll
+                        for (int kk = 0; kk < 2 * t; ++kk) {
+                            const uint32_t a = tbase + tm_arow(t) + 8 * kk;
+                            const uint64_t boff = (uint64_t)((dablk(t, 0) * 1024 + 512 * kk) >> 4);
+                            tc::mma_tf32_ts(tbase + TM_XQ + 16 * (t - 1), a, dq0 + boff, id16, true);
+                            tc::mma_tf32_ts(tbase + TM_XK + 16 * (t - 1), a, dk0 + boff, id16, true);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 1; j < NBLK; ++j) {
+                        const uint32_t idj = tc::idesc_tf32(128, 16 * j);
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const uint64_t off = (bcol_off(j) + 256 * kk) >> 4;
+                            tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AQB + 16 * (j - 1) + 8 * kk,
+                                            cq0 + off, idj, true);
+                            tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AKBB + 16 * (j - 1) + 8 * kk,
+                                            ck0 + off, idj, true);
+                        }
+                    }
+                    tc::mma_commit(mbar2);
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int r = RMID - 1; r >= BC / 2; --r) {
+                if constexpr (!FACTOR) accq[r] = acck[r] = 0.f;
+                diag_row(r);
+            }
         }
         if constexpr (FACTOR) {
 #pragma unroll
@@ -793,7 +1001,7 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         }
 
         // ---- cross terms: wait for the MMAs, apply the post-factors ----
-        ok &= tc::mbar_wait(mbar, (uint32_t)it & 1u, SPIN_LIMIT);
+        ok &= tc::mbar_wait(SPLIT ? mbar2 : mbar, (uint32_t)it & 1u, SPIN_LIMIT);
         tc::fence_after_sync();
         if (i > 0) {
             float f[BC], x[BC];
@@ -916,10 +1124,12 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
 cudaError_t make_maps(const BwdArgs &a, TmaMaps *tm);
 cudaError_t num_sms(int *n, int *dev);
 
-template <typename io_t, bool ACCUM, bool FOLD, bool EMIT, bool VARLEN, bool FACTOR>
+template <typename io_t, bool ACCUM, bool FOLD, bool EMIT, bool VARLEN, bool FACTOR,
+          bool SPLIT = false>
 cudaError_t launch_typed(const BwdArgs &a, cudaStream_t stream) {
-    auto kern = kda_intra_bwd_tc_kernel<io_t, ACCUM, FOLD, EMIT, VARLEN, FACTOR>;
-    const int smem_bytes = FOLD ? SM_TOTAL_FOLD : SM_TOTAL;
+    auto kern = kda_intra_bwd_tc_kernel<io_t, ACCUM, FOLD, EMIT, VARLEN, FACTOR, SPLIT>;
+    static_assert(!(FOLD && SPLIT), "no shared-memory layout for both");
+    const int smem_bytes = FOLD ? SM_TOTAL_FOLD : SPLIT ? SM_TOTAL_SPLIT : SM_TOTAL;
     static volatile int smem_set[kMaxDev];  // this instantiation's attribute, per device
     int nsm = 0, dev = 0;
     cudaError_t e = num_sms(&nsm, &dev);
@@ -957,6 +1167,13 @@ cudaError_t launch_opts(const BwdArgs &a, cudaStream_t stream) {
                          : launch_typed<io_t, true, false, EMIT, VARLEN, FACTOR>(a, stream);
     return a.fold_dg ? launch_typed<io_t, false, true, EMIT, VARLEN, FACTOR>(a, stream)
                      : launch_typed<io_t, false, false, EMIT, VARLEN, FACTOR>(a, stream);
+}
+
+// The split-TF32 cross sums: fixed-length units, no other option but grouped value
+// heads.
+template <typename io_t>
+cudaError_t launch_split(const BwdArgs &a, cudaStream_t stream) {
+    return launch_typed<io_t, false, false, false, false, false, true>(a, stream);
 }
 
 // Every option combination of one q/k element type, one sequence layout and one

@@ -18,6 +18,7 @@ struct BwdArgs {
     bool fold_dg = false;  // dg as its inclusive reverse cumsum inside each chunk
     bool emit_io = false;  // dq, dk written in the q/k element type
     bool factor_diag = false;  // diagonal blocks' lower-left quadrant through row 8
+    bool split = false;        // cross sums in split TF32 (FP32-level accuracy)
     unsigned *dbg = nullptr;   // bounds-checked debug build: the caller's flag word
     // variable-length sequences packed along T (B == 1): sequence n holds tokens
     // [cu_seqlens[n], cu_seqlens[n+1]); chunk c of the launch is chunk

@@ -69,6 +69,7 @@ extern "C" {
 
 /*
  * ABI versions (kda_abi_version() returns the loaded library's):
+ *   9  kda_intra_bwd_opts_t gains split_tf32 (appended; the struct grew)
  *   8  kda_intra_bwd_host_static, KDA_HOST_STATIC_MAX_BYTES, KDA_ERR_TOO_LARGE
  *   7  kda_debug_checks, kda_debug_set_flags (the bounds-checked debug build)
  *   6  kda_intra_bwd_opts_t gains factor_diag (appended; the struct grew)
@@ -83,7 +84,7 @@ extern "C" {
  * must check at start-up that kda_abi_version() equals the KDA_ABI_VERSION it was
  * compiled with (the Python binding refuses to load any other version).
  */
-#define KDA_ABI_VERSION 8
+#define KDA_ABI_VERSION 9
 #define KDA_BT 64  /* chunk length */
 #define KDA_BC 16  /* sub-block length inside a chunk */
 #define KDA_K 128  /* head dimension */
@@ -244,8 +245,17 @@ kda_status_t kda_intra_bwd_host_static(const void *q, const void *k, const float
  *                  quadrant costs four FMAs per (r, s, d) instead of an exp2 and seven
  *                  FP32 operations (about 4% less kernel time).  The result differs
  *                  from the exact form by rounding only; same accuracy contract.
+ *   split_tf32     1: the cross-sub-block sums in split TF32 for FP32-level accuracy:
+ *                  every tensor-core operand x is cut into hi = tf32(x) and lo = x - hi
+ *                  and each product is taken as A_hi B_hi + A_hi B_lo + A_lo B_hi on the
+ *                  tensor cores with FP32 accumulation (the dropped A_lo B_lo is about
+ *                  2^-22 of the product); the diagonal blocks stay on the FP32 pipes.
+ *                  Accuracy max|err| / max|ref| <= 1e-4 per output tensor, as
+ *                  kda_intra_bwd_fp32, at about half its time.  Fixed-length sequences
+ *                  only, and no other option but HV; anything else is KDA_ERR_OPTION.
  *
- * Runs on the tensor-core path (the same accuracy contract as kda_intra_bwd).
+ * Runs on the tensor-core path (the same accuracy contract as kda_intra_bwd, except
+ * with split_tf32).
  */
 typedef struct {
     int HV;
@@ -260,6 +270,7 @@ typedef struct {
     int num_seqs;
     int num_chunks;
     int factor_diag;
+    int split_tf32;
 } kda_intra_bwd_opts_t;
 
 kda_status_t kda_intra_bwd_ex(const void *q, const void *k, const float *g,

@@ -12,8 +12,9 @@ import oracle
 NAMES = ("dq", "dk", "db", "dg")
 ARGS = ("q", "k", "g", "beta", "dAqk", "dAkk")
 
-# max|err| / max|ref| per output tensor
-TOL = {"kda_intra_bwd": 2e-3, "kda_intra_bwd_fp32": 1e-4}
+# max|err| / max|ref| per output tensor; "split_tf32" is kda_intra_bwd_ex with the
+# split-TF32 cross sums, held to the FP32 path's tolerance
+TOL = {"kda_intra_bwd": 2e-3, "kda_intra_bwd_fp32": 1e-4, "split_tf32": 1e-4}
 PATHS = tuple(TOL)
 
 
@@ -22,6 +23,8 @@ def to_device(inp: dict, device="cuda") -> dict:
 
 
 def run(path: str, dev: dict, **kw):
+    if path == "split_tf32":
+        return kda.kda_intra_bwd_ex(*(dev[n] for n in ARGS), split_tf32=True, **kw)
     fn = getattr(kda, path)
     return fn(*(dev[n] for n in ARGS), **kw)
 

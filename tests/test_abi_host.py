@@ -174,6 +174,17 @@ def test_ex_rejections(lib):
     assert ex_call(lib, q=0) == ERR_NULL
 
 
+def test_ex_split_tf32_rejections(lib):
+    """split_tf32 takes no other option but HV (and only the values 0 and 1)."""
+    assert ex_call(lib, ins={"split_tf32": 2}) == 9
+    assert ex_call(lib, ins={"split_tf32": -1}) == 9
+    assert ex_call(lib, fold=1, ins={"split_tf32": 1}) == 9
+    assert ex_call(lib, emit=1, ins={"split_tf32": 1}) == 9
+    assert ex_call(lib, ins={"split_tf32": 1, "factor_diag": 1}) == 9
+    assert ex_call(lib, ins={"split_tf32": 1, "db_in": BASE + 8 * SPAN}) == 9
+    assert ex_call(lib, ins={"split_tf32": 1, **varlen_ins()}) == 9
+
+
 def test_ex_accepts_in_place_and_reaches_the_device(lib):
     import torch
     if torch.cuda.is_available():
@@ -183,6 +194,7 @@ def test_ex_accepts_in_place_and_reaches_the_device(lib):
     assert ex_call(lib, H=2, HV=4, fold=1, ins=ins) in (ERR_CUDA, ERR_DEVICE)
     assert ex_call(lib, emit=1) in (ERR_CUDA, ERR_DEVICE)
     assert ex_call(lib, ins={"factor_diag": 1}) in (ERR_CUDA, ERR_DEVICE)
+    assert ex_call(lib, H=2, HV=4, ins={"split_tf32": 1}) in (ERR_CUDA, ERR_DEVICE)
     # NULL options behave like kda_intra_bwd
     args = fake_args()[:-1]
     assert lib.kda_intra_bwd_ex(*args, None, ctypes.c_void_p(0)) in (ERR_CUDA, ERR_DEVICE)

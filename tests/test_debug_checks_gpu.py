@@ -48,6 +48,7 @@ def test_fast_and_fp32_paths(shape, dtype):
     _same_under_checks(lambda: kda.kda_intra_bwd(*args))
     _same_under_checks(lambda: kda.kda_intra_bwd_fp32(*args))
     _same_under_checks(lambda: kda.kda_intra_bwd_ex(*args, factor_diag=True))
+    _same_under_checks(lambda: kda.kda_intra_bwd_ex(*args, split_tf32=True))
     _same_under_checks(lambda: kda.kda_intra_fwd(*args[:4]))
 
 

@@ -56,6 +56,7 @@ def _inputs():
     ("kda_intra_bwd", "kda_intra_bwd_tc_kernel"),
     ("kda_intra_bwd_fp32", "kda_intra_bwd_fp32_kernel"),
     ("kda_intra_bwd_ex", "kda_intra_bwd_tc_kernel"),
+    ("split_tf32", "kda_intra_bwd_tc_kernel"),
     ("kda_intra_fwd", "kda_intra_fwd_tc_kernel"),
 ])
 def test_entry_point_launches_its_own_kernel(entry, kernel, tmp_path):
@@ -65,8 +66,10 @@ def test_entry_point_launches_its_own_kernel(entry, kernel, tmp_path):
         call = lambda: kda.kda_intra_fwd(*ins[:4], *outs)  # noqa: E731
     else:
         outs = list(kda._outputs(ins[0], None, None, None, None))
-        extra = {"factor_diag": True} if entry == "kda_intra_bwd_ex" else {}
-        call = lambda: getattr(kda, entry)(*ins, *outs, **extra)  # noqa: E731
+        extra = {"factor_diag": True} if entry == "kda_intra_bwd_ex" else \
+            {"split_tf32": True} if entry == "split_tf32" else {}
+        fn = kda.kda_intra_bwd_ex if entry == "split_tf32" else getattr(kda, entry)
+        call = lambda: fn(*ins, *outs, **extra)  # noqa: E731
     call()  # first call outside the trace: the module loads, attributes are set
     names = _kernels(call, tmp_path)
     ours = [n for n in names if kernel in n]

@@ -193,7 +193,7 @@ def test_misaligned_pointer_is_a_status_not_a_fault():
     bad.copy_(dev["g"])
     for path in _gpu.PATHS:
         with pytest.raises(kda.KdaError, match="ALIGN"):
-            getattr(kda, path)(dev["q"], dev["k"], bad, dev["beta"], dev["dAqk"], dev["dAkk"])
+            _gpu.run(path, {**dev, "g": bad})
 
 
 def test_sampled_units_match_full_launch():
