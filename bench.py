@@ -571,12 +571,17 @@ def run_ours(args, cfg):
             extra["db_in"] = torch.randn(cfg.B, cfg.T, cfg.H, generator=gen).to(dev)
         extra["factor_diag"] = args.factor_diag
         extra["split_tf32"] = args.split_tf32
-        outs = list(kda.kda_intra_bwd_ex(*ins, **extra, fold_dg=args.fold_dg,
-                                         dqdk_io_dtype=args.io_dtype_out))
+        if args.in_place:
+            if not args.accumulate or args.io_dtype_out:
+                raise SystemExit("--in-place needs --accumulate and fp32 outputs")
+            outs = [extra["dq_in"], extra["dk_in"], extra["db_in"], extra["dg_in"]]
+        else:
+            outs = list(kda.kda_intra_bwd_ex(*ins, **extra, fold_dg=args.fold_dg,
+                                             dqdk_io_dtype=args.io_dtype_out))
         opts = {"value_heads_per_qk_head": args.gva, "accumulate": args.accumulate,
                 "fold_dg": args.fold_dg, "dqdk_io_dtype": args.io_dtype_out,
                 "varlen": args.varlen, "factor_diag": args.factor_diag,
-                "split_tf32": args.split_tf32}
+                "split_tf32": args.split_tf32, "in_place": args.in_place}
 
         def step():
             kda.kda_intra_bwd_ex(*ins, *outs, **extra, fold_dg=args.fold_dg,
@@ -716,6 +721,8 @@ def main():
                    help="value heads per q/k head (kda_intra_bwd_ex); heads stay H")
     p.add_argument("--accumulate", action="store_true",
                    help="add incoming dq/dk/dg/db in-kernel (kda_intra_bwd_ex)")
+    p.add_argument("--in-place", action="store_true",
+                   help="with --accumulate: the incoming gradients are the outputs themselves")
     p.add_argument("--fold-dg", action="store_true",
                    help="dg as its chunk-local reverse cumsum (kda_intra_bwd_ex)")
     p.add_argument("--io-dtype-out", action="store_true",

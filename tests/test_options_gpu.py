@@ -71,6 +71,37 @@ def test_incoming_gradients_partial_and_in_place():
         assert torch.equal(a, b), f"in-place {n} differs from out-of-place"
 
 
+@pytest.mark.parametrize("fold", [False, True])
+@pytest.mark.parametrize("varlen", [False, True])
+def test_in_place_accumulation_matches_out_of_place(fold, varlen):
+    """dq_in, dk_in, dg_in given as the outputs themselves: the stores add to them in L2
+    (dg_in is read before the fold); bitwise the out-of-place result, for whole and short
+    chunks.  Partly in place (dq only) takes the loading path and agrees too."""
+    if varlen:
+        lens = [70, 1, 130, 64]
+        B, T = 1, sum(lens)
+        cpu, cu = kda_inputs.make_varlen_inputs(lens, 3, seed=47)
+        extra = {"cu_seqlens": cu.cuda()}
+    else:
+        B, T = 2, 192
+        cpu = kda_inputs.make_inputs(B, T, 3, seed=47)
+        extra = {}
+    ins = incoming(B, T, 3, seed=48)
+    dev = _gpu.to_device(cpu)
+    ref = kda.kda_intra_bwd_ex(*(dev[n] for n in _gpu.ARGS), fold_dg=fold,
+                               **{n: v.cuda() for n, v in ins.items()}, **extra)
+    bufs = {n: v.cuda() for n, v in ins.items()}
+    out = kda.kda_intra_bwd_ex(*(dev[n] for n in _gpu.ARGS), dq=bufs["dq_in"], dk=bufs["dk_in"],
+                               db=bufs["db_in"], dg=bufs["dg_in"], fold_dg=fold, **bufs, **extra)
+    for n, a, b in zip(_gpu.NAMES, out, ref):
+        assert torch.equal(a, b), f"in-place {n} differs from out-of-place"
+    part = {n: v.cuda() for n, v in ins.items()}
+    dq = part["dq_in"]
+    got = kda.kda_intra_bwd_ex(*(dev[n] for n in _gpu.ARGS), dq=dq, fold_dg=fold, **part, **extra)
+    for n, a, b in zip(_gpu.NAMES, got, ref):
+        assert torch.equal(a, b), f"partly in-place {n} differs from out-of-place"
+
+
 def test_fold_dg():
     cpu = kda_inputs.make_inputs(2, 256, 3, seed=45)
     _gpu.assert_close(run_ex(cpu, fold_dg=True), ref_ex(cpu, fold_dg=True), TOL, "fold_dg")
