@@ -210,7 +210,11 @@ kda_status_t kda_intra_bwd_host_static(const void *q, const void *k, const float
  *                  (grouped value attention).  0 means HV = H.  Must be a multiple of H.
  *   dq_in, dk_in,  optional [B,T,HV,128] fp32 gradients added in-kernel to dq, dk, dg
  *   dg_in          (NULL = none).  May be the same pointer as the matching output
- *                  (in-place accumulation); any other overlap is rejected.
+ *                  (in-place accumulation); any other overlap is rejected.  When dq_in,
+ *                  dk_in and (without fold_dg) dg_in are all their outputs, the kernel
+ *                  reads none of them: its stores add to them in L2 (red.global.add, one
+ *                  rounding as otherwise, but subnormal sums flush to zero), the fastest
+ *                  way to accumulate.
  *   db_in          optional [B,T,HV] fp32 added to db; may equal db.
  *   fold_dg        1: dg comes back as its inclusive reverse cumsum inside each
  *                  64-token chunk, out[t] = sum_{t' >= t in t's chunk} dg[t'] (the
