@@ -185,6 +185,46 @@ def test_host_entry_point_pipelined_pieces(pinned_host):
         assert torch.equal(a, b.cpu()), n
 
 
+def test_host_entry_point_from_several_threads():
+    """Four host threads call kda_intra_bwd_host at once, each with its own buffers,
+    workspace and stream (the calls share the library's internal copy streams and
+    events, taken under a per-device lock; ctypes releases the GIL): every result is
+    bitwise the device path's."""
+    import threading
+    B, T, H = 1, 2048, 4
+    jobs = []
+    for n in range(4):
+        cpu = kda_inputs.make_inputs(B, T, H, seed=150 + n)
+        host = {k: v.pin_memory() for k, v in cpu.items()}
+        outs = [torch.empty(B, T, H, 128).pin_memory(), torch.empty(B, T, H, 128).pin_memory(),
+                torch.empty(B, T, H).pin_memory(), torch.empty(B, T, H, 128).pin_memory()]
+        ws = torch.empty(kda.kda_intra_bwd_host_workspace_bytes(B, T, H, torch.bfloat16),
+                         dtype=torch.uint8, device="cuda")
+        jobs.append((cpu, host, outs, ws, torch.cuda.Stream()))
+    errors = []
+
+    def work(job):
+        cpu, host, outs, ws, stream = job
+        try:
+            for _ in range(3):
+                kda.kda_intra_bwd_host(*(host[n] for n in _gpu.ARGS), *outs, workspace=ws,
+                                       stream=stream)
+            stream.synchronize()
+        except Exception as e:  # pragma: no cover - reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(j,)) for j in jobs]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for cpu, host, outs, ws, stream in jobs:
+        ref = _gpu.run("kda_intra_bwd", _gpu.to_device(cpu))
+        for n, a, b in zip(_gpu.NAMES, outs, ref):
+            assert torch.equal(a, b.cpu()), n
+
+
 def test_misaligned_pointer_is_a_status_not_a_fault():
     cpu = kda_inputs.make_inputs(1, 64, 1, seed=18)
     dev = _gpu.to_device(cpu)
