@@ -45,9 +45,8 @@ constexpr int FM_STG = 2 * FSTAGE;              // Aqk, Akk tiles: 2 x 2 swizzle
 constexpr int FM_B = FM_STG + 32768;            // B_1, B_2, B_3: [16t][128] tf32, K-major
 constexpr int FM_BETA = FM_B + 49152;           // f32 [2][64]
 constexpr int FM_DIAG = FM_BETA + 512;          // f32 [2][512]: diagonal sums until the epilogue
-constexpr int FM_BAR = FM_DIAG + 2 * 512 * 4;   // full[2], mma, staging free
-constexpr int FM_CNT = FM_BAR + 32;             // operand counter
-constexpr int FM_TSLOT = FM_CNT + 8;
+constexpr int FM_BAR = FM_DIAG + 2 * 512 * 4;   // full[2], mma, staging free, operands
+constexpr int FM_TSLOT = FM_BAR + 40;
 constexpr int FM_META = FM_TSLOT + 8;           // varlen: per stage {first token row, valid rows}
 constexpr int FM_LUT = FM_META + 16;            // varlen: the same for this CTA's units,
 constexpr int LUT_BATCH = 32;                   // two batches of 32
@@ -216,7 +215,6 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + FM_BAR);
     uint64_t *mbar = full + 2;
     uint64_t *stg_free = full + 3;  // completes once per unit: the last tiles have left
-    uint32_t *ops_count = reinterpret_cast<uint32_t *>(smem + FM_CNT);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + FM_TSLOT);
     int *meta = reinterpret_cast<int *>(smem + FM_META);
     unsigned char *stg = smem + FM_STG;
@@ -226,9 +224,9 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
     if (tid == 0) {
         tc::mbar_init(&full[0], FULL_ARRIVALS);
         tc::mbar_init(&full[1], FULL_ARRIVALS);
-        tc::mbar_init(mbar, 1);
+        tc::mbar_init(mbar, 3);                 // one commit per MMA chain
         tc::mbar_init(stg_free, 1);
-        ops_count[0] = 0u;
+        tc::mbar_init(stg_free + 1, 16);        // operands written, one arrival per warp
         tc::prefetch_tmap(&tm.q);
         tc::prefetch_tmap(&tm.k);
         tc::prefetch_tmap(&tm.g);
@@ -360,7 +358,9 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
                                             (sr >> 3) * 128 + (sr & 7) * 16) = o;
             }
         }
-        // operands complete; the last warp to get here issues the 48 MMAs.  Thread 0
+        // operands complete: every warp arrives on the operands barrier; warps 13, 14
+        // and 15 each wait for it and issue one of the three MMA chains, so the warp
+        // that refilled the stage (warp 0, last at this point) issues none.  Thread 0
         // also releases the staging once the previous unit's tiles have left it.
         tc::tmem_wait_st();
         tc::fence_proxy_async_smem();
@@ -371,22 +371,21 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
         }
         __syncwarp();
         {
-            uint32_t prev = 0;
-            if (lane == 0) prev = tc::atomic_add_acq_rel_smem(ops_count, 1u);
-            prev = __shfl_sync(0xffffffffu, prev, 0);
-            if ((prev % 16u) == 15u) {
+            if (lane == 0) tc::mbar_arrive(stg_free + 1);
+            // warps 13, 14, 15 each issue one MMA chain (target block t = warp - 12) once
+            // every warp's operands are written
+            if (warp >= 13) {
+                ok &= tc::mbar_wait(stg_free + 1, (uint32_t)it & 1u, SPIN_LIMIT);
                 tc::fence_after_sync();
                 if (tc::elect_one()) {
+                    const int t = warp - 12;
+                    const uint64_t b0 =
+                        tc::smem_desc(tc::smem_u32(smem + FM_B + boff(t)), 256 * t, 128);
+                    const uint32_t id = tc::idesc_tf32(128, 16 * t);
 #pragma unroll
-                    for (int t = 1; t < NBLK; ++t) {
-                        const uint64_t b0 =
-                            tc::smem_desc(tc::smem_u32(smem + FM_B + boff(t)), 256 * t, 128);
-                        const uint32_t id = tc::idesc_tf32(128, 16 * t);
-#pragma unroll
-                        for (int kk = 0; kk < KD / 8; ++kk)
-                            tc::mma_tf32_ts(tbase + tm_d(t), tbase + 8 * kk,
-                                            b0 + (uint64_t)((512 * t * kk) >> 4), id, kk > 0);
-                    }
+                    for (int kk = 0; kk < KD / 8; ++kk)
+                        tc::mma_tf32_ts(tbase + tm_d(t), tbase + 8 * kk,
+                                        b0 + (uint64_t)((512 * t * kk) >> 4), id, kk > 0);
                     tc::mma_commit(mbar);
                 }
             }

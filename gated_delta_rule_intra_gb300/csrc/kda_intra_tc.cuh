@@ -51,6 +51,7 @@ namespace tcimpl {
 
 constexpr int TC_THREADS = 512;
 constexpr int TC_WARPS = TC_THREADS / 32;
+constexpr int MMA_WARPS = 3;  // warps 13..15 issue the MMAs
 
 // ---- shared memory: two input stages + single-buffered derived operands ----
 // dA tiles: the ten lower 16x16 blocks (t, j <= t) of a unit, block (t, j) at
@@ -70,8 +71,8 @@ constexpr int SM_BCQ = 2 * STAGE_BYTES;      // dAqk blocks of target j transpos
 constexpr int SM_BCK = SM_BCQ + 6144;
 constexpr int SM_DBP = SM_BCK + 6144;        // db partials f32 [4][64]
 constexpr int SM_FULL = SM_DBP + 1024;       // 2 stage-full mbarriers
-constexpr int SM_MMA = SM_FULL + 16;         // MMAs-done mbarrier
-constexpr int SM_CNT = SM_MMA + 8;           // operand counter, unit-done counter
+constexpr int SM_MMA = SM_FULL + 16;         // MMAs-done mbarrier, operands-written mbarrier
+constexpr int SM_CNT = SM_MMA + 16;          // (unused), unit-done counter
 constexpr int SM_TSLOT = SM_CNT + 8;
 constexpr int SM_META = SM_TSLOT + 8;        // varlen: per stage {first token row, valid rows}
 constexpr int SM_LUT = SM_META + 16;         // varlen: {first row, valid rows} of this
@@ -89,7 +90,7 @@ constexpr int SM_SPLIT_Q = (SM_TOTAL + 1023) / 1024 * 1024;
 constexpr int SM_SPLIT_K = SM_SPLIT_Q + 6144;
 constexpr int SM_SPLIT_CQ = SM_SPLIT_K + 6144;
 constexpr int SM_SPLIT_CK = SM_SPLIT_CQ + 6144;
-constexpr int SM_SPLIT_BAR = SM_SPLIT_CK + 6144;  // pass-2 MMAs-done mbarrier, pass-2 counter
+constexpr int SM_SPLIT_BAR = SM_SPLIT_CK + 6144;  // pass-2 MMAs-done and operands mbarriers
 constexpr int SM_TOTAL_SPLIT = SM_SPLIT_BAR + 16;
 // extra shared memory of the fold_dg variant: the per-row dg bank [64][128] and the
 // per-(sub-block, channel) totals, double-buffered by unit parity
@@ -324,24 +325,22 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
     const int r0 = i * BC;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM_FULL);
     uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + SM_MMA);
-    uint32_t *ops_count = reinterpret_cast<uint32_t *>(smem + SM_CNT);
-    uint32_t *done_count = ops_count + 1;
+    uint32_t *done_count = reinterpret_cast<uint32_t *>(smem + SM_CNT) + 1;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + SM_TSLOT);
     float *sdbp = reinterpret_cast<float *>(smem + SM_DBP);
     const long long stride = gridDim.x;
 
     uint64_t *mbar2 = reinterpret_cast<uint64_t *>(smem + SM_SPLIT_BAR);  // SPLIT only
-    uint32_t *ops2_count = reinterpret_cast<uint32_t *>(smem + SM_SPLIT_BAR + 8);
     if (warp == 0) tc::tmem_alloc(tslot, TM_COLS);
     if (tid == 0) {
         tc::mbar_init(&full[0], FULL_ARRIVALS);
         tc::mbar_init(&full[1], FULL_ARRIVALS);
-        tc::mbar_init(mbar, 1);
+        tc::mbar_init(mbar, MMA_WARPS);        // one commit per issuing warp
+        tc::mbar_init(mbar + 1, TC_WARPS);     // operands written, one arrival per warp
         if constexpr (SPLIT) {
-            tc::mbar_init(mbar2, 1);
-            ops2_count[0] = 0u;
+            tc::mbar_init(mbar2, MMA_WARPS);
+            tc::mbar_init(mbar2 + 1, TC_WARPS);
         }
-        ops_count[0] = 0u;
         done_count[0] = 0u;
         tc::prefetch_tmap(&tm.q);
         tc::prefetch_tmap(&tm.k);
@@ -640,79 +639,87 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             }
         }
 
-        // operands complete: TMEM stores landed, smem stores visible to the tensor core;
-        // the last warp to get here issues the 36 MMAs (no thread waits for the others)
+        // operands complete: TMEM stores landed, smem stores visible to the tensor core.
+        // Every warp arrives on the operands barrier and goes on to its diagonal block;
+        // warps 13, 14 and 15 (sub-block 3, the lightest prescale) wait for it and issue
+        // the MMAs, each a third of the accumulator chains.  No warp issues on its way
+        // from its own operands to its diagonal, and the three issue in parallel.
         tc::tmem_wait_st();
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
         __syncwarp();
         uint32_t prev = 0;
-        if (lane == 0) prev = tc::atomic_add_acq_rel_smem(ops_count, 1u);
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        // The branch is warp-uniform so the descriptor arithmetic stays on the uniform
-        // datapath; one elected lane issues.
-        if ((prev % TC_WARPS) == TC_WARPS - 1) {
-            tc::fence_after_sync();
+        if (lane == 0) tc::mbar_arrive(mbar + 1);
+        // The unit's MMAs of one pass, the chains of warp w (each accumulator chain stays
+        // on one thread: Xq_t, Xk_t over K = 16t, P_j over the q and beta*k sides):
+        //   w = 13: Xq_3, Xk_3;  w = 14: Xq_2, Xk_2, P_1;  w = 15: Xq_1, Xk_1, P_2, P_3
+        // (12 MMAs each).  pass 1: A (SPLIT: A_hi) times the dA blocks (SPLIT: then times
+        // their low parts); pass 2 (SPLIT): A_lo times the dA blocks.
+        auto issue_chains = [&](const int pass) {
             const uint64_t dq0 = tc::smem_desc(tc::smem_u32(st + ST_DQ), 256, 128);
             const uint64_t dk0 = tc::smem_desc(tc::smem_u32(st + ST_DK), 256, 128);
             const uint64_t cq0 = tc::smem_desc(tc::smem_u32(smem + SM_BCQ), 128, 512);
             const uint64_t ck0 = tc::smem_desc(tc::smem_u32(smem + SM_BCK), 128, 512);
+            const uint64_t ql0 = tc::smem_desc(tc::smem_u32(smem + SM_SPLIT_Q), 256, 128);
+            const uint64_t kl0 = tc::smem_desc(tc::smem_u32(smem + SM_SPLIT_K), 256, 128);
+            const uint64_t cql0 = tc::smem_desc(tc::smem_u32(smem + SM_SPLIT_CQ), 128, 512);
+            const uint64_t ckl0 = tc::smem_desc(tc::smem_u32(smem + SM_SPLIT_CK), 128, 512);
             const uint32_t id16 = tc::idesc_tf32(128, 16);
-            if (tc::elect_one()) {
-#pragma unroll
-                for (int t = 1; t < NBLK; ++t) {
-#pragma unroll
-                    for (int kk = 0; kk < 2 * t; ++kk) {
-                        const uint32_t a = tbase + tm_arow(t) + 8 * kk;
-                        const uint64_t boff = (uint64_t)((dablk(t, 0) * 1024 + 512 * kk) >> 4);
-                        tc::mma_tf32_ts(tbase + TM_XQ + 16 * (t - 1), a, dq0 + boff, id16, kk > 0);
-                        tc::mma_tf32_ts(tbase + TM_XK + 16 * (t - 1), a, dk0 + boff, id16, kk > 0);
-                    }
-                }
-#pragma unroll
-                for (int j = 1; j < NBLK; ++j) {
-                    const uint32_t idj = tc::idesc_tf32(128, 16 * j);
-#pragma unroll
-                    for (int kk = 0; kk < 2; ++kk)
+            const bool lo_b = SPLIT && pass == 1;  // also the low parts of B
+            const bool first = pass == 1;          // the chain's first MMA overwrites D
+            auto xchain = [&](const int t, const bool kside) {
+                const uint64_t bhi = kside ? dk0 : dq0, blo = kside ? kl0 : ql0;
+                const uint32_t d = tbase + (kside ? TM_XK : TM_XQ) + 16 * (t - 1);
+                for (int kk = 0; kk < 2 * t; ++kk)
+                    tc::mma_tf32_ts(d, tbase + tm_arow(t) + 8 * kk,
+                                    bhi + (uint64_t)((dablk(t, 0) * 1024 + 512 * kk) >> 4), id16,
+                                    !first || kk > 0);
+                if (lo_b)
+                    for (int kk = 0; kk < 2 * t; ++kk)
+                        tc::mma_tf32_ts(d, tbase + tm_arow(t) + 8 * kk,
+                                        blo + (uint64_t)(((t * (t - 1) / 2) * 1024 + 512 * kk) >> 4),
+                                        id16, true);
+            };
+            auto pchain = [&](const int j) {
+                const uint32_t idj = tc::idesc_tf32(128, 16 * j);
+                for (int kk = 0; kk < 2; ++kk)
+                    tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AQB + 16 * (j - 1) + 8 * kk,
+                                    cq0 + ((bcol_off(j) + 256 * kk) >> 4), idj, !first || kk > 0);
+                for (int kk = 0; kk < 2; ++kk)
+                    tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AKBB + 16 * (j - 1) + 8 * kk,
+                                    ck0 + ((bcol_off(j) + 256 * kk) >> 4), idj, true);
+                if (lo_b)
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const uint64_t off = (bcol_off(j) + 256 * kk) >> 4;
                         tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AQB + 16 * (j - 1) + 8 * kk,
-                                        cq0 + ((bcol_off(j) + 256 * kk) >> 4), idj, kk > 0);
-#pragma unroll
-                    for (int kk = 0; kk < 2; ++kk)
+                                        cql0 + off, idj, true);
                         tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AKBB + 16 * (j - 1) + 8 * kk,
-                                        ck0 + ((bcol_off(j) + 256 * kk) >> 4), idj, true);
-                }
-                if constexpr (SPLIT) {  // pass 1, second half: A_hi times the low parts of B
-                    const uint64_t ql0 = tc::smem_desc(tc::smem_u32(smem + SM_SPLIT_Q), 256, 128);
-                    const uint64_t kl0 = tc::smem_desc(tc::smem_u32(smem + SM_SPLIT_K), 256, 128);
-                    const uint64_t cql0 = tc::smem_desc(tc::smem_u32(smem + SM_SPLIT_CQ), 128, 512);
-                    const uint64_t ckl0 = tc::smem_desc(tc::smem_u32(smem + SM_SPLIT_CK), 128, 512);
-#pragma unroll
-                    for (int t = 1; t < NBLK; ++t) {
-#pragma unroll
-                        for (int kk = 0; kk < 2 * t; ++kk) {
-                            const uint32_t a = tbase + tm_arow(t) + 8 * kk;
-                            const uint64_t boff = (uint64_t)(((t * (t - 1) / 2) * 1024 + 512 * kk) >> 4);
-                            tc::mma_tf32_ts(tbase + TM_XQ + 16 * (t - 1), a, ql0 + boff, id16, true);
-                            tc::mma_tf32_ts(tbase + TM_XK + 16 * (t - 1), a, kl0 + boff, id16, true);
-                        }
+                                        ckl0 + off, idj, true);
                     }
-#pragma unroll
-                    for (int j = 1; j < NBLK; ++j) {
-                        const uint32_t idj = tc::idesc_tf32(128, 16 * j);
-#pragma unroll
-                        for (int kk = 0; kk < 2; ++kk) {
-                            const uint64_t off = (bcol_off(j) + 256 * kk) >> 4;
-                            tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AQB + 16 * (j - 1) + 8 * kk,
-                                            cql0 + off, idj, true);
-                            tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AKBB + 16 * (j - 1) + 8 * kk,
-                                            ckl0 + off, idj, true);
-                        }
-                    }
+            };
+            if (tc::elect_one()) {
+                if (warp == 13) {
+                    xchain(3, false);
+                    xchain(3, true);
+                } else if (warp == 14) {
+                    xchain(2, false);
+                    xchain(2, true);
+                    pchain(1);
+                } else {
+                    xchain(1, false);
+                    xchain(1, true);
+                    pchain(2);
+                    pchain(3);
                 }
-                tc::mma_commit(mbar);
+                tc::mma_commit(pass == 1 ? mbar : mbar2);
             }
+            __syncwarp();
+        };
+        if (warp >= TC_WARPS - MMA_WARPS) {
+            ok &= tc::mbar_wait(mbar + 1, (uint32_t)it & 1u, SPIN_LIMIT);
+            tc::fence_after_sync();
+            issue_chains(1);
         }
-        __syncwarp();
 
         // ---- diagonal block, two source rows at a time in packed FP32x2: one exp2 per
         // (r, s, d), shared by both sides (FACTOR: in the two 8x8 triangles, with the
@@ -964,41 +971,11 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             tc::tmem_wait_st();
             tc::fence_before_sync();
             __syncwarp();
-            uint32_t prev2 = 0;
-            if (lane == 0) prev2 = tc::atomic_add_acq_rel_smem(ops2_count, 1u);
-            prev2 = __shfl_sync(0xffffffffu, prev2, 0);
-            if ((prev2 % TC_WARPS) == TC_WARPS - 1) {
+            if (lane == 0) tc::mbar_arrive(mbar2 + 1);
+            if (warp >= TC_WARPS - MMA_WARPS) {
+                ok &= tc::mbar_wait(mbar2 + 1, (uint32_t)it & 1u, SPIN_LIMIT);
                 tc::fence_after_sync();
-                const uint64_t dq0 = tc::smem_desc(tc::smem_u32(st + ST_DQ), 256, 128);
-                const uint64_t dk0 = tc::smem_desc(tc::smem_u32(st + ST_DK), 256, 128);
-                const uint64_t cq0 = tc::smem_desc(tc::smem_u32(smem + SM_BCQ), 128, 512);
-                const uint64_t ck0 = tc::smem_desc(tc::smem_u32(smem + SM_BCK), 128, 512);
-                const uint32_t id16 = tc::idesc_tf32(128, 16);
-                if (tc::elect_one()) {  // pass 2: A_lo times the high parts of B
-#pragma unroll
-                    for (int t = 1; t < NBLK; ++t) {
-#pragma unroll
-                        for (int kk = 0; kk < 2 * t; ++kk) {
-                            const uint32_t a = tbase + tm_arow(t) + 8 * kk;
-                            const uint64_t boff = (uint64_t)((dablk(t, 0) * 1024 + 512 * kk) >> 4);
-                            tc::mma_tf32_ts(tbase + TM_XQ + 16 * (t - 1), a, dq0 + boff, id16, true);
-                            tc::mma_tf32_ts(tbase + TM_XK + 16 * (t - 1), a, dk0 + boff, id16, true);
-                        }
-                    }
-#pragma unroll
-                    for (int j = 1; j < NBLK; ++j) {
-                        const uint32_t idj = tc::idesc_tf32(128, 16 * j);
-#pragma unroll
-                        for (int kk = 0; kk < 2; ++kk) {
-                            const uint64_t off = (bcol_off(j) + 256 * kk) >> 4;
-                            tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AQB + 16 * (j - 1) + 8 * kk,
-                                            cq0 + off, idj, true);
-                            tc::mma_tf32_ts(tbase + tm_p(j), tbase + TM_AKBB + 16 * (j - 1) + 8 * kk,
-                                            ck0 + off, idj, true);
-                        }
-                    }
-                    tc::mma_commit(mbar2);
-                }
+                issue_chains(2);
             }
             __syncwarp();
 #pragma unroll
