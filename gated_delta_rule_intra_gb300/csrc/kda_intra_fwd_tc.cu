@@ -164,6 +164,58 @@ __device__ __forceinline__ void load_unit(unsigned char *st, float *sbeta, uint6
     tc::cp_async_mbar_arrive_noinc(full);
 }
 
+// The same copies spread over warps 0..8 (part = warp): warp 0 arms the barrier and
+// issues the first q box, warps 1..7 one box each, warp 8 the beta copies; every warp
+// of the CTA leaves the unit's barrier together, so no warp carries all of them.
+template <typename io_t, bool VARLEN>
+__device__ __forceinline__ void load_unit_part(int part, unsigned char *st, float *sbeta,
+                                               uint64_t *full, int *meta, const FwdMaps &tm,
+                                               const float *__restrict__ beta, long long u,
+                                               int T, int H, const FwdExtras &ex, int lane,
+                                               const int *known) {
+    int row, h, len = BT;
+    if constexpr (VARLEN) {
+        row = known[0];
+        len = known[1];
+        h = (int)((unsigned)u % (unsigned)H);
+    } else {
+        const Unit x = decode_unit(u, H, T / BT);
+        row = x.b * T + x.c * BT;
+        h = x.h;
+    }
+    if (part < 8) {
+        if (lane == 0) {
+            if (part == 0) {
+                if constexpr (VARLEN) {
+                    meta[0] = row;
+                    meta[1] = len;
+                }
+                tc::mbar_arrive_expect_tx(full, FSTAGE_TX_BYTES);
+            }
+            if (part < 2)
+                tc::tma_load_3d(st + FS_Q + part * 8192, &tm.q, 64 * part, h / ex.G, row, full);
+            else if (part < 4)
+                tc::tma_load_3d(st + FS_K + (part - 2) * 8192, &tm.k, 64 * (part - 2), h / ex.G,
+                                row, full);
+            else
+                tc::tma_load_3d(st + FS_G + (part - 4) * 8192, &tm.g, 32 * (part - 4), h, row,
+                                full);
+        }
+        return;
+    }
+    const float *b0 = beta + ((size_t)row * H + h);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int r = lane + 32 * e;
+        const uint32_t s = tc::smem_u32(sbeta + r);
+        const bool take = r < len && dbg_ok(ex.dbg, (size_t)(row + r) * H + h, ex.nrows, DBG_LOAD);
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(s),
+                     "l"(take ? b0 + (size_t)r * H : beta), "r"(take ? 4 : 0)
+                     : "memory");
+    }
+    tc::cp_async_mbar_arrive_noinc(full);
+}
+
 // Sum of v[0..15] over the 16 lanes of a half-warp, transposed: lane (lane & 15) = j
 // ends with the total of index j in v[0].  15 shuffles.
 __device__ __forceinline__ float reduce16(float (&v)[16], int lane) {
@@ -556,13 +608,13 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
         if constexpr (VARLEN) {
             if (warp == 0 && ((it + 2) % LUT_BATCH) == 0) lookup_batch(it + 2 + LUT_BATCH);
         }
-        if (warp == 0 && u + 2 * stride < units)
-            load_unit<io_t, VARLEN>(st, reinterpret_cast<float *>(smem + FM_BETA) + 64 * sidx,
-                                    &full[sidx], meta + 2 * sidx, tm, beta, u + 2 * stride, T,
-                                    H, ex, lane,
-                                    VARLEN ? lut + (((it + 2) / LUT_BATCH) & 1) * 2 * LUT_BATCH +
-                                                 2 * ((it + 2) % LUT_BATCH)
-                                           : nullptr);
+        if (warp <= 8 && u + 2 * stride < units)
+            load_unit_part<io_t, VARLEN>(warp, st,
+                                         reinterpret_cast<float *>(smem + FM_BETA) + 64 * sidx,
+                                         &full[sidx], meta + 2 * sidx, tm, beta, u + 2 * stride,
+                                         T, H, ex, lane,
+                                         lut + (((it + 2) / LUT_BATCH) & 1) * 2 * LUT_BATCH +
+                                             2 * ((it + 2) % LUT_BATCH));
     }
 
     dbg_flag(ex.dbg, !ok, DBG_WAIT);
