@@ -105,6 +105,17 @@ cudaError_t encode_maps(const BwdArgs &a, TmaMaps *tm) {
         if ((e = encode(&tm->g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.g, dims, str, box)) !=
             cudaSuccess)
             return e;
+        const cuuint32_t box16[3] = {KD, 1, BC};
+        if ((e = encode(&tm->g16, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.g, dims, str, box16)) !=
+            cudaSuccess)
+            return e;
+    }
+    {
+        const cuuint64_t dims[3] = {KD, HQ, rows};
+        const cuuint64_t str[2] = {KD * 2, HQ * KD * 2};
+        const cuuint32_t box16[3] = {KD, 1, BC};
+        if ((e = encode(&tm->q16, io, 3, a.q, dims, str, box16)) != cudaSuccess) return e;
+        if ((e = encode(&tm->k16, io, 3, a.k, dims, str, box16)) != cudaSuccess) return e;
     }
     // no L2 promotion for dA: a promoted fetch would also pull the rows' unused upper part
     const CUtensorMapL2promotion l2 = CU_TENSOR_MAP_L2_PROMOTION_NONE;

@@ -103,6 +103,8 @@ static_assert(ST_DQ % 1024 == 0 && ST_DK % 1024 == 0, "dA tiles alignment");
 
 constexpr uint32_t STAGE_TX_BYTES = 2 * BT * KD * 2 + BT * KD * 4 + 2 * 10 * 1024;
 constexpr uint32_t FULL_ARRIVALS = 1 + 32;  // expect_tx by lane 0 + beta copies by 32 lanes
+constexpr uint32_t SLICE_TX_BYTES = 2 * BC * KD * 2 + BC * KD * 4;  // q, k, g rows of a sub-block
+constexpr uint32_t FULL_ARRIVALS_SLICED = NBLK * (1 + 32);
 
 __host__ __device__ constexpr int dablk(int t, int j) { return t * (t + 1) / 2 + j; }
 
@@ -126,6 +128,7 @@ constexpr uint32_t SPIN_LIMIT = 1u << 22;
 // (t, 0..t) in one box of 16 rows x 16(t+1) columns, landing in the operand layout.
 struct TmaMaps {
     CUtensorMap q, k, g, daqk[NBLK], dakk[NBLK];
+    CUtensorMap q16, k16, g16;  // 16-row boxes: one sub-block's rows (fixed length)
 };
 
 // Options of the extended entry point.  H in the kernel is the number of heads of g,
@@ -295,6 +298,35 @@ __device__ __forceinline__ void load_unit(unsigned char *st, uint64_t *full, int
     tc::cp_async_mbar_arrive_noinc(full);
 }
 
+// Fixed-length units, one sub-block's share of the copies into a stage: rows
+// 16i..16i+15 of q, k and g and row-block i's dA blocks (five TMA tiles from lane 0),
+// and those rows' beta (16 four-byte copies).  Per sub-block the stage barrier counts
+// one arrival carrying the share's bytes and 32 copy arrivals.
+__device__ __forceinline__ void load_slice(unsigned char *st, uint64_t *full, const TmaMaps &tm,
+                                           const float *__restrict__ beta, long long u, int H,
+                                           const Extras ex, int lane, int i) {
+    const unsigned qq = (unsigned)u / (unsigned)H;
+    const int h = (int)((unsigned)u - qq * (unsigned)H);
+    const int row = BT * (int)qq + BC * i;  // first token row of the share
+    if (lane == 0) {
+        tc::mbar_arrive_expect_tx(full, SLICE_TX_BYTES + 2048u * (uint32_t)(i + 1));
+        tc::tma_load_3d(st + ST_Q + i * BC * KD * 2, &tm.q16, 0, h / ex.G, row, full);
+        tc::tma_load_3d(st + ST_K + i * BC * KD * 2, &tm.k16, 0, h / ex.G, row, full);
+        tc::tma_load_3d(st + ST_G + i * BC * KD * 4, &tm.g16, 0, h, row, full);
+        tc::tma_load_5d(st + ST_DQ + dablk(i, 0) * 1024, &tm.daqk[i], 0, 0, row >> 3, 0, h, full);
+        tc::tma_load_5d(st + ST_DK + dablk(i, 0) * 1024, &tm.dakk[i], 0, 0, row >> 3, 0, h, full);
+    }
+    if (lane < BC) {
+        const size_t bi = (size_t)(row + lane) * H + h;
+        unsigned char *dst = st + ST_BETA + (BC * i + lane) * 4;
+        if (dbg_ok(ex.dbg, bi, ex.nrows, DBG_LOAD))
+            cp_async4(dst, beta + bi);
+        else
+            cp_async4_zfill(dst, beta, false);
+    }
+    tc::cp_async_mbar_arrive_noinc(full);
+}
+
 // ACCUM: add the optional incoming gradients of Extras (1: loaded and added; 2: dq_in,
 // dk_in and, without FOLD, dg_in are the outputs themselves, and the stores add to them
 // in L2 with red.global.add instead: nothing to load); FOLD: return dg as its
@@ -332,9 +364,12 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
 
     uint64_t *mbar2 = reinterpret_cast<uint64_t *>(smem + SM_SPLIT_BAR);  // SPLIT only
     if (warp == 0) tc::tmem_alloc(tslot, TM_COLS);
+    // SPLIT: each sub-block refills its own rows of a stage as soon as its four warps
+    // are done with them (measured faster there; slower on the other paths)
+    constexpr bool SLICED = SPLIT && !VARLEN;
     if (tid == 0) {
-        tc::mbar_init(&full[0], FULL_ARRIVALS);
-        tc::mbar_init(&full[1], FULL_ARRIVALS);
+        tc::mbar_init(&full[0], SLICED ? FULL_ARRIVALS_SLICED : FULL_ARRIVALS);
+        tc::mbar_init(&full[1], SLICED ? FULL_ARRIVALS_SLICED : FULL_ARRIVALS);
         tc::mbar_init(mbar, MMA_WARPS);        // one commit per issuing warp
         tc::mbar_init(mbar + 1, TC_WARPS);     // operands written, one arrival per warp
         if constexpr (SPLIT) {
@@ -345,6 +380,11 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         tc::prefetch_tmap(&tm.q);
         tc::prefetch_tmap(&tm.k);
         tc::prefetch_tmap(&tm.g);
+        if constexpr (SLICED) {
+            tc::prefetch_tmap(&tm.q16);
+            tc::prefetch_tmap(&tm.k16);
+            tc::prefetch_tmap(&tm.g16);
+        }
 #pragma unroll
         for (int t = 0; t < NBLK; ++t) {
             tc::prefetch_tmap(&tm.daqk[t]);
@@ -398,7 +438,14 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             e[1] = x.len;
         }
     };
-    if (warp == 0) {  // the first two units of this CTA
+    if (SLICED && warp == 0) {  // the first two units of this CTA
+        for (int s = 0; s < 2; ++s) {
+            const long long us = blockIdx.x + s * stride;
+            if (us < units)
+                for (int j = 0; j < NBLK; ++j)
+                    load_slice(smem + s * STAGE_BYTES, &full[s], tm, beta, us, H, ex, lane, j);
+        }
+    } else if (warp == 0) {  // the first two units of this CTA
         const long long u0 = blockIdx.x;
         if (u0 < units) load_unit<VARLEN>(smem, &full[0], meta, tm, beta, u0, T, H, ex, lane);
         if (u0 + stride < units)
@@ -1053,6 +1100,14 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         db_rows(0);
 #undef KDA_EL
         tc::named_bar_sync(1 + i, 128);
+        if constexpr (SLICED) {
+            // the sub-block's rows of the stage are read no more in this unit (every
+            // other sub-block's reads of them came before this unit's MMAs completed)
+            if ((warp & 3) == 1 && u + 2 * stride < units) {
+                tc::fence_proxy_async_smem();
+                load_slice(st, &full[sidx], tm, beta, u + 2 * stride, H, ex, lane, i);
+            }
+        }
         if ((warp & 3) == 0 && lane < BC && (!VARLEN || r0 + lane < ulen)) {
             const int row = r0 + lane;
             // recomputed here rather than kept live across the unit (register budget)
@@ -1085,18 +1140,21 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             }
         }
 
-        // ---- unit done: the last warp releases the stage and refills it ----
-        tc::fence_before_sync();
-        __syncwarp();
-        prev = 0;
-        if (lane == 0) prev = tc::atomic_add_acq_rel_smem(done_count, 1u);
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        if ((prev % TC_WARPS) == TC_WARPS - 1 && u + 2 * stride < units) {
-            tc::fence_proxy_async_smem();
-            load_unit<VARLEN>(st, &full[sidx], meta + 2 * sidx, tm, beta, u + 2 * stride, T, H,
-                              ex, lane,
-                              lut + (((it + 2) / LUT_BATCH) & 1) * 2 * LUT_BATCH +
-                                  2 * ((it + 2) % LUT_BATCH));
+        // ---- unit done: the last warp releases the stage and refills it (SLICED: the
+        // sub-blocks have refilled their rows above) ----
+        if constexpr (!SLICED) {
+            tc::fence_before_sync();
+            __syncwarp();
+            prev = 0;
+            if (lane == 0) prev = tc::atomic_add_acq_rel_smem(done_count, 1u);
+            prev = __shfl_sync(0xffffffffu, prev, 0);
+            if ((prev % TC_WARPS) == TC_WARPS - 1 && u + 2 * stride < units) {
+                tc::fence_proxy_async_smem();
+                load_unit<VARLEN>(st, &full[sidx], meta + 2 * sidx, tm, beta, u + 2 * stride,
+                                  T, H, ex, lane,
+                                  lut + (((it + 2) / LUT_BATCH) & 1) * 2 * LUT_BATCH +
+                                      2 * ((it + 2) % LUT_BATCH));
+            }
         }
     }
 
