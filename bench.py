@@ -145,6 +145,23 @@ def ncu_traffic(kernel: str, workload: str):
         return None
 
 
+def summary_name(args, workload: str):
+    """Which committed ncu summary covers this run's launch: the plain launch of each
+    path on its workload, and on their own the split-TF32, factor_diag and
+    variable-length launches of the backward (whose summaries carry the option's name
+    or the variable-length workload's).  Other options have none (None)."""
+    if args.gva > 1 or args.accumulate or args.fold_dg or args.io_dtype_out:
+        return None
+    picked = [n for n, on in (("split_tf32", args.split_tf32),
+                               ("factor_diag", args.factor_diag),
+                               ("varlen", args.varlen)) if on]
+    if not picked:
+        return workload
+    if len(picked) > 1 or args.path != "kda_intra_bwd":
+        return None
+    return workload if picked == ["varlen"] else f"{picked[0]}_{workload}"
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
 
@@ -671,8 +688,8 @@ def run_ours(args, cfg):
         clocks["kcycles_per_step"] = ms_per_step * clocks["sm_mhz"]
     peak, peak_kind = hbm_peak()
     kname = KERNEL_NAMES[args.path]
-    # the committed summaries cover the plain launch of each path only
-    traffic = None if extended else ncu_traffic(kname, cfg.name)
+    summary = summary_name(args, cfg.name)
+    traffic = ncu_traffic(kname, summary) if summary else None
     line = {
         "metric": METRIC,
         "value": world * cfg.tokens_heads / (ms_per_step / 1e3),

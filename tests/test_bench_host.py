@@ -48,6 +48,30 @@ def test_traffic_is_null_when_the_summary_is_for_other_sources(monkeypatch):
     assert bench.ncu_traffic(name, workload) is None
 
 
+def test_option_launches_find_their_own_summaries():
+    """The split-TF32, factor_diag and variable-length launches of the backward report
+    the traffic of their own summaries; other options and combinations report none."""
+    import argparse
+    base = dict(gva=1, accumulate=False, fold_dg=False, io_dtype_out=False, varlen=False,
+                factor_diag=False, split_tf32=False, path="kda_intra_bwd")
+    a = lambda **kw: argparse.Namespace(**{**base, **kw})  # noqa: E731
+    w = kda_inputs.CONFIGS[kda_inputs.HEADLINE].name
+    assert bench.summary_name(a(), w) == w
+    assert bench.summary_name(a(path="kda_intra_fwd"), w) == w
+    assert bench.summary_name(a(split_tf32=True), w) == "split_tf32_" + w
+    assert bench.summary_name(a(factor_diag=True), w) == "factor_diag_" + w
+    assert bench.summary_name(a(varlen=True), "varlen_T32768_H16") == "varlen_T32768_H16"
+    for kw in (dict(gva=4), dict(accumulate=True), dict(fold_dg=True), dict(io_dtype_out=True),
+               dict(varlen=True, factor_diag=True), dict(varlen=True, path="kda_intra_fwd")):
+        assert bench.summary_name(a(**kw), w) is None, kw
+    # each named summary exists and is for the current sources
+    for summary in (w, "split_tf32_" + w, "factor_diag_" + w, "varlen_T32768_H16"):
+        traffic = bench.ncu_traffic("kda_intra_bwd_tc_kernel", summary)
+        if traffic is None:
+            pytest.skip("a committed summary predates the current sources")
+        assert traffic > 0.9 * 1.5e9
+
+
 def test_config_selection():
     assert bench.parse_configs("2") == [kda_inputs.HEADLINE]
     assert bench.parse_configs("gate_stress") == [kda_inputs.GATE_STRESS]
