@@ -949,8 +949,13 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
             if ((lane & 3) == 0) sdbp[(warp & 3) * BT + r0 + rbase + (lane >> 2)] = v[0];
         };
 
+        // the first rows' incoming gradients: fetched here, or, with the fold (the fullest
+        // registers), only after the post-factors, just before the first output row
+        // (measured faster each way)
+        if constexpr (!FOLD) {
 #pragma unroll
-        for (int r = BC - 1; r >= BC - AHEAD; --r) fetch_in(r);
+            for (int r = BC - 1; r >= BC - AHEAD; --r) fetch_in(r);
+        }
         // SPLIT: rows 15..12, then the second MMA pass is prepared, then rows 11..8
         constexpr int RMID = SPLIT ? 3 * BC / 4 : BC / 2;
 #pragma unroll
@@ -1089,6 +1094,10 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         }
 
         // ---- rows 15..8 are complete: write them; then rows 7..0 ----
+        if constexpr (FOLD) {
+#pragma unroll
+            for (int r = BC - 1; r >= BC - AHEAD; --r) fetch_in(r);
+        }
 #pragma unroll
         for (int r = BC - 1; r >= BC / 2; --r) out_row(r);
         db_rows(BC / 2);
