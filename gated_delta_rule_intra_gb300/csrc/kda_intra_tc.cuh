@@ -458,15 +458,17 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
     int it = 0;
     // Head of the current unit, advanced by stride mod H each iteration.  With u = q H + h
     // the unit's first [token * H + head] row is 64 u - 63 h, so no unit needs a division.
-    // (The incoming-gradient variant keeps the decode: its registers are fuller.)
+    // (The instantiations that load incoming gradients keep the decode: their registers are
+    // fuller.  Measured each way.)
+    constexpr bool DECODE = ACCUM == 1 || (ACCUM == 2 && FOLD);
     const unsigned dhh = (unsigned)stride % (unsigned)H;
     unsigned hh = (unsigned)blockIdx.x % (unsigned)H;
     auto unit_row = [&](const long long u, const int r) -> size_t {  // fixed-length: row r
-        if constexpr (ACCUM) return grow(decode_unit(u, H, T / BT), r, T, H);
+        if constexpr (DECODE) return grow(decode_unit(u, H, T / BT), r, T, H);
         else return (size_t)64 * (size_t)u - (size_t)63 * hh + (size_t)r * H;
     };
     auto unit_head = [&](const long long u) -> unsigned {
-        if constexpr (ACCUM) return (unsigned)u % (unsigned)H;
+        if constexpr (DECODE) return (unsigned)u % (unsigned)H;
         else return hh;
     };
     for (long long u = blockIdx.x; u < units;
