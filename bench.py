@@ -502,7 +502,7 @@ def end_to_end(kda, args, cfg, cpu, outs, stream, dev, world):
     return res
 
 
-E2E_ROUNDS = 3
+E2E_ROUNDS = 5
 LINK_MIN_BYTES = 256 << 20  # below this a copy's fixed cost, not the link, sets the time
 LINK_PIECE = 96 << 20
 
