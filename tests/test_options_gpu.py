@@ -49,6 +49,16 @@ def test_grouped_value_heads_fp16_stress():
     _gpu.assert_close(run_ex(cpu), ref_ex(cpu), TOL, "GVA fp16 stress")
 
 
+@pytest.mark.parametrize("G", [2, 4])
+def test_split_tf32_with_grouped_value_heads(G):
+    """The split-TF32 cross sums with HV = G*H value heads (q/k read per group), held to
+    the FP32 path's tolerance; 3 q/k heads x 64 chunks so that the persistent CTAs walk
+    several units each and the group index wraps across them."""
+    cpu = grouped_inputs(2, 2048, 3, G, seed=60 + G)
+    got = run_ex(cpu, split_tf32=True)
+    _gpu.assert_close(got, ref_ex(cpu), _gpu.TOL["split_tf32"], f"split_tf32 G={G}")
+
+
 def test_incoming_gradients_added():
     cpu = kda_inputs.make_inputs(2, 192, 3, seed=41)
     ins = incoming(2, 192, 3, seed=42)
