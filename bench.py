@@ -106,15 +106,41 @@ KERNEL_SOURCES = {
 }
 
 
+def code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments and blank lines (string and character
+    literals kept, trailing blanks dropped): what the compiler sees, so that an edit of
+    comments alone leaves a kernel's hash unchanged."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c and text[j] != "\n":
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.rstrip() for line in "".join(out).split("\n"))
+    return "\n".join(line for line in lines if line)
+
+
 def source_hash(kernel: str) -> str:
-    """Hash of the source files one kernel is compiled from (ties an ncu summary to
-    the code it measured)."""
+    """Hash of the code (comments left out) of the source files one kernel is compiled
+    from: ties an ncu summary to the code it measured."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_intra_gb300", "csrc")
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, f), "rb") as fh:
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             h.update(f.encode())
-            h.update(fh.read())
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

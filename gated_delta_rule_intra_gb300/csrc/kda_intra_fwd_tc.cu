@@ -295,7 +295,7 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
     const uint32_t tbase = *tslot;
 
     // VARLEN: lane j of warp 0 looks up the row range of this CTA's unit k0 + j, for the
-    // refills of a whole batch of units at once (warp 0 also does every refill)
+    // refills of a whole batch of units at once (warps 0..8 share every refill)
     int *lut = reinterpret_cast<int *>(smem + FM_LUT);
     auto lookup_batch = [&](const int k0) {
         const long long uk = blockIdx.x + (long long)(k0 + lane) * stride;
@@ -411,8 +411,8 @@ kda_intra_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const float *__restr
             }
         }
         // operands complete: every warp arrives on the operands barrier; warps 13, 14
-        // and 15 each wait for it and issue one of the three MMA chains, so the warp
-        // that refilled the stage (warp 0, last at this point) issues none.  Thread 0
+        // and 15 each wait for it and issue one of the three MMA chains, so none of the
+        // warps that refilled the stage (0..8, last at this point) issues them.  Thread 0
         // also releases the staging once the previous unit's tiles have left it.
         tc::tmem_wait_st();
         tc::fence_proxy_async_smem();

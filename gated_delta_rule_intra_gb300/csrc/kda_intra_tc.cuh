@@ -4,13 +4,14 @@
 // round-robin.  Two shared-memory stages hold the inputs of consecutive units; the
 // tensor memory accelerator fills a stage while the other one is being computed.
 // There is no CTA-wide barrier inside the unit loop: warps hand work to each other
-// through mbarriers and two shared counters, so fast warps run ahead into the
-// next unit instead of idling:
+// through mbarriers and a shared counter, so fast warps run ahead into the next unit
+// instead of idling:
 //   * the stage-full mbarrier completes when a unit's TMA tiles and beta have landed;
-//   * the last warp to finish writing its tensor-core operands issues the unit's 36
-//     MMAs (every other warp goes straight on to the diagonal blocks);
-//   * the last warp to finish a unit releases its stage and loads the unit after
-//     next into it;
+//   * every warp arrives on an operands mbarrier once its tensor-core operands are
+//     written and goes on to its diagonal block; warps 13, 14 and 15 wait for it and
+//     issue the unit's 36 MMAs, 12 each, in parallel;
+//   * the last warp to finish a unit (the shared counter) releases its stage and loads
+//     the unit after next into it (SPLIT: each sub-block loads its own rows);
 //   * the per-row sum for dbeta meets across the four warps of a sub-block at a
 //     128-thread named barrier.
 //
@@ -967,7 +968,7 @@ kda_intra_bwd_tc_kernel(const __grid_constant__ TmaMaps tm, const float *__restr
         }
         if constexpr (SPLIT) {
             // pass 1 done: the A operands it read are replaced by their low parts
-            // (recomputed exactly as in the prescale), then the last warp issues pass 2
+            // (recomputed exactly as in the prescale), then warps 13..15 issue pass 2
             ok &= tc::mbar_wait(mbar, (uint32_t)it & 1u, SPIN_LIMIT);
             tc::fence_after_sync();
             if (i < NBLK - 1) {

@@ -72,6 +72,19 @@ def test_option_launches_find_their_own_summaries():
         assert traffic > 0.9 * 1.5e9
 
 
+def test_source_hash_sees_code_only():
+    """A kernel's hash (which ties an ncu summary to its sources) ignores comments and
+    blank lines, keeps literals, and changes with the code."""
+    a = "int x = 1; // one\n/* two\n lines */\nint y;\n"
+    b = "int x = 1;\n\n// another comment\n   \nint y;   \n"
+    assert bench.code_only(a) == bench.code_only(b) == "int x = 1;\nint y;"
+    assert bench.code_only("int x = 2;") != bench.code_only("int x = 1;")
+    s = 'const char *s = "// kept /* too */"; char c = \'/\';'
+    assert bench.code_only(s) == s
+    for kernel in bench.KERNEL_SOURCES:
+        assert len(bench.source_hash(kernel)) == 16
+
+
 def test_config_selection():
     assert bench.parse_configs("2") == [kda_inputs.HEADLINE]
     assert bench.parse_configs("gate_stress") == [kda_inputs.GATE_STRESS]
